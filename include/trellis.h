@@ -1,0 +1,170 @@
+/*
+ * trellis.h -- C ABI of libtrellis.so: linear layers over packed trellis-coded
+ * (QTIP "1MAD") weights on NVIDIA GB300 (sm_103a).
+ *
+ * Format (from the "trellis-linear.ts" diff page, mlx-bun 0.2.0 -> 0.4.0, the
+ * file's header comment): a weight matrix is stored as a uint32 bitstream
+ * codes[rows][cols*k/32] plus one fp16 scale per stored row.  Each stored row
+ * is a sequence of blocks of T positions (T*k/32 words per block).  The state
+ * of position t of a block is the L-bit window starting at bit (T-1-t)*k of
+ * the block, bits read least-significant first inside little-endian words and
+ * wrapping to the block's first word.  A state s decodes with the 1MAD code:
+ * x = s*34038481 + 76625530 (mod 2^32), y = (sum of the four bytes of x) - 510,
+ * value = y / 147.800537109375, weight = value * scale[row].
+ *
+ * axis = 1: coded along the input dimension; the stored matrix is W [out, in]
+ *           (rows = out features, cols = in features).
+ * axis = 0: coded along the output dimension; the stored matrix is W^T
+ *           [in, out] (rows = in features, cols = out features).
+ *
+ * Conventions for every call:
+ *   - All array arguments are DEVICE pointers to memory the caller allocated
+ *     and owns; the library never allocates, frees or retains them.  Inputs
+ *     are read only.  Every pointer must be 16-byte aligned.
+ *   - bf16 and fp16 values travel as their 16-bit storage patterns (uint16_t).
+ *   - Arrays are dense and row-major in the shapes given below.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream) and return after the launch.  The library keeps no
+ *     state between calls except a per-device cache of launch attributes;
+ *     calls are thread-safe.
+ *   - The return value is TRELLIS_OK or a negative trellis_status.  On every
+ *     error except TRELLIS_ECUDA nothing was launched and no memory touched;
+ *     TRELLIS_ECUDA reports the CUDA error seen at launch.
+ *
+ * Supported geometry of the GPU kernels: k in {2, 3, 4}, L = 16 or 12,
+ * T = 256, rows >= 1, cols a positive multiple of T.  (The pages' own fast
+ * paths assume L = 12 and T = 256; the measured workloads use L = 16.)
+ */
+#ifndef TRELLIS_H
+#define TRELLIS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Geometry of one packed matrix (TrellisGeometry on the "trellis-linear.ts"
+ * page: {k, L, T, axis, rows, cols}; rows/cols are the STORED matrix's). */
+typedef struct trellis_geom {
+  int32_t k;     /* bits per weight */
+  int32_t L;     /* window (trellis state) length in bits */
+  int32_t T;     /* positions per block */
+  int32_t axis;  /* 1 or 0, see above */
+  int64_t rows;  /* stored rows */
+  int64_t cols;  /* coded positions per stored row */
+} trellis_geom_t;
+
+typedef void *trellis_stream_t; /* a cudaStream_t */
+
+enum trellis_status {
+  TRELLIS_OK = 0,
+  TRELLIS_EGEOM = -1,      /* unsupported or inconsistent geometry */
+  TRELLIS_EM = -2,         /* M outside the call's range */
+  TRELLIS_EALIGN = -3,     /* a pointer is not 16-byte aligned */
+  TRELLIS_EAXIS = -4,      /* geometry axis does not fit the call */
+  TRELLIS_EWORKSPACE = -5, /* workspace missing, misaligned or too small */
+  TRELLIS_ECUDA = -6,      /* CUDA reported an error at launch */
+  TRELLIS_ENULL = -7,      /* a required pointer is NULL */
+  TRELLIS_EDEVICE = -8     /* no usable sm_103 device is current */
+};
+
+/* Version of this interface (major*100 + minor). */
+int trellis_abi_version(void);
+
+/* Static description of a status code; never NULL. */
+const char *trellis_status_string(int status);
+
+/* 0 if the GPU kernels support the geometry, else TRELLIS_EGEOM.  Pure host
+ * check (trellisGeometry's rules plus the kernels' supported set). */
+int trellis_check_geom(const trellis_geom_t *g);
+
+/*
+ * trellis_expand_bf16 -- decode the whole stored matrix
+ * ("trellis-linear.ts": expandTrellis / EXPAND_SOURCE; "trellis-vector-
+ * expand.ts").  out[r][c] = bf16(value(s(r,c)) * scale[r]), where value is
+ * the correctly rounded fp32 quotient y / 147.800537109375, the product is
+ * rounded to fp32 and then to bf16 (nearest, ties to even).  Bit-exact.
+ *   codes  [rows][cols*k/32] uint32     scales [rows] fp16
+ *   out    [rows][cols] bf16, in STORED order (for axis 0 this is W^T).
+ * Any axis.  Writes every element of out.
+ */
+int trellis_expand_bf16(const uint32_t *codes, const uint16_t *scales, uint16_t *out,
+                        const trellis_geom_t *g, trellis_stream_t stream);
+
+/*
+ * trellis_matvec_axis1 -- decode-fused matvec for M = 1..4 input rows over
+ * an axis-1 matrix ("trellis-linear.ts": TrellisLinear.forward for M <= 4,
+ * REDUCE_SOURCE; "trellis-shared-m.ts" for M = 2..4).
+ *   out[m][r] = bf16( sum_c w(r,c) * x[m][c] ),  w = fp32 value * scale[r]
+ * (the pages' default packed numerics: no bf16 rounding of the weight),
+ * accumulated in fp32 in any order.
+ *   codes [rows][cols*k/32]   scales [rows]   x [M][cols] bf16   out [M][rows] bf16
+ * Requires g->axis == 1 and 1 <= M <= 4.
+ */
+int trellis_matvec_axis1(const uint32_t *codes, const uint16_t *scales, const uint16_t *x,
+                         uint16_t *out, int M, const trellis_geom_t *g, trellis_stream_t stream);
+
+/*
+ * trellis_matvec_axis0 -- decode-fused matvec for M = 1..4 input rows over
+ * an axis-0 matrix, i.e. a stored W^T ("trellis-linear.ts": the scatter path
+ * of TrellisLinear.forward, SCATTER_SOURCE and its partial fold;
+ * "trellis-balanced-scatter.ts" and "trellis-shared-scatter.ts").
+ *   out[m][c] = bf16( sum_r w(r,c) * x[m][r] ),  w = fp32 value * scale[r]
+ * The sum over stored rows is split across thread blocks; each block writes
+ * fp32 partial sums to `workspace` and the last block to finish a column
+ * block folds the partials in a fixed order (deterministic) and stores bf16.
+ *   codes [rows][cols*k/32]   scales [rows]   x [M][rows] bf16   out [M][cols] bf16
+ *   workspace: device memory of at least trellis_workspace_bytes(M, g) bytes,
+ *   16-byte aligned, ZERO-FILLED before its first use; every call leaves it
+ *   ready for the next one.  Calls that share a workspace must not overlap
+ *   in time (put them on one stream).
+ * Requires g->axis == 0 and 1 <= M <= 4.
+ */
+int trellis_matvec_axis0(const uint32_t *codes, const uint16_t *scales, const uint16_t *x,
+                         uint16_t *out, int M, const trellis_geom_t *g, void *workspace,
+                         size_t workspace_bytes, trellis_stream_t stream);
+
+/* Bytes of workspace trellis_matvec_axis0 needs for (M, g); 0 if the
+ * geometry or M is unsupported. */
+size_t trellis_workspace_bytes(int M, const trellis_geom_t *g);
+
+/*
+ * trellis_gateup_swiglu -- fused gate/up projections with the SwiGLU
+ * activation for M = 1..4 ("trellis-linear.ts": fusedGateUpSwiglu /
+ * GATEUP_SOURCE; "trellis-shared-m.ts": GATEUP_SHARED_M_SOURCE).  Both
+ * matrices are decoded once per call, x is read once, and the gate and up
+ * vectors are never stored:
+ *   g = bf16(sum_c wg(r,c) x[m][c]),  u = bf16(sum_c wu(r,c) x[m][c])
+ *   sig = bf16(1 / (1 + exp(-g))),  silu = bf16(g * sig),
+ *   out[m][r] = bf16(silu * u)      (fp32 arithmetic between the casts)
+ * Both matrices share the geometry g (axis 1; same k, L, T, rows, cols).
+ *   gcodes, ucodes [rows][cols*k/32]   gscales, uscales [rows]
+ *   x [M][cols] bf16   out [M][rows] bf16
+ */
+int trellis_gateup_swiglu(const uint32_t *gcodes, const uint16_t *gscales, const uint32_t *ucodes,
+                          const uint16_t *uscales, const uint16_t *x, uint16_t *out, int M,
+                          const trellis_geom_t *g, trellis_stream_t stream);
+
+/*
+ * trellis_gemm_prefill -- prefill GEMM over an axis-1 matrix for any M >= 1
+ * (intended for M > 4) ("trellis-tiled-prefill.ts": tiledTrellisPrefill and
+ * the expand + matmul path of TrellisLinear.forward).  Weight tiles are
+ * decoded into shared memory as bf16 (the expand numerics: bf16 of the
+ * correctly rounded value times the scale), x tiles arrive by TMA, and the
+ * 5th-generation tensor cores (tcgen05, accumulators in tensor memory)
+ * compute
+ *   out[m][r] = bf16( sum_c e(r,c) * x[m][c] ),  e = the bf16 expand weight,
+ * accumulated in fp32.
+ *   codes [rows][cols*k/32]   scales [rows]   x [M][cols] bf16   out [M][rows] bf16
+ * Requires g->axis == 1, M >= 1, and cols a multiple of 64.
+ */
+int trellis_gemm_prefill(const uint32_t *codes, const uint16_t *scales, const uint16_t *x,
+                         uint16_t *out, int M, const trellis_geom_t *g, trellis_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TRELLIS_H */

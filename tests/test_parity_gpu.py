@@ -1,0 +1,204 @@
+"""Parity of the CUDA path (through the C ABI) against the oracle.
+
+Small cases are compared element by element in full: they span several
+blocks, ragged row counts (not a multiple of 32), one-block rows, and M = 1..4.
+Full-size cases (the 27B-class MLP shapes, in the launch configuration the
+bench times) are compared on sampled rows or columns that the oracle computes
+one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+from trellis_coded_weight_gb300 import binding as tb
+from trellis_coded_weight_gb300 import inputs
+from util import bf16_bits, check_band, to_dev_bf16, to_dev_f16, to_dev_u32
+
+pytestmark = pytest.mark.gpu
+L, T = 16, 256
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from trellis_coded_weight_gb300 import build
+    build.build()
+    tb.load()
+
+
+def _sample(n, count, seed):
+    rng = np.random.default_rng(seed)
+    idx = set(rng.choice(n, size=min(count, n), replace=False).tolist()) | {0, n - 1}
+    return np.array(sorted(idx), dtype=np.int64)
+
+
+# ------------------------------------------------------------------ expand
+
+@pytest.mark.parametrize("k", [2, 3, 4])
+@pytest.mark.parametrize("rows,cols", [(1, 256), (37, 768), (64, 2048)])
+def test_expand_bit_exact_small(oracle_mod, k, rows, cols):
+    codes, scales, _ = inputs.make_linear(rows, cols, k, 1, seed_codes=11 + k, seed_scales=12)
+    g = tb.Geometry(k, L, T, 1, rows, cols)
+    out = tb.expand_bf16(to_dev_u32(codes), to_dev_f16(scales), g)
+    torch.cuda.synchronize()
+    assert np.array_equal(bf16_bits(out), oracle_mod.expand_bf16(codes, scales, k, L, T))
+
+
+@pytest.mark.parametrize("k", [2, 3, 4])
+def test_expand_bit_exact_full_size_sampled(oracle_mod, k):
+    rows, cols = 17408, 5120
+    codes, scales, _ = inputs.make_linear(rows, cols, k, 1)
+    g = tb.Geometry(k, L, T, 1, rows, cols)
+    out = bf16_bits(tb.expand_bf16(to_dev_u32(codes), to_dev_f16(scales), g))
+    idx = _sample(rows, 48, k)
+    assert np.array_equal(out[idx], oracle_mod.expand_bf16(codes, scales, k, L, T, rows=idx))
+
+
+def test_expand_L12(oracle_mod):
+    codes, scales, _ = inputs.make_linear(40, 512, 3, 1, seed_codes=77)
+    out = tb.expand_bf16(to_dev_u32(codes), to_dev_f16(scales), tb.Geometry(3, 12, T, 1, 40, 512))
+    assert np.array_equal(bf16_bits(out), oracle_mod.expand_bf16(codes, scales, 3, 12, T))
+
+
+# ------------------------------------------------------------------ axis 1
+
+@pytest.mark.parametrize("k", [2, 3, 4])
+@pytest.mark.parametrize("M", [1, 2, 3, 4])
+@pytest.mark.parametrize("rows,cols", [(1, 256), (45, 768), (100, 1280)])
+def test_matvec_axis1_small(oracle_mod, k, M, rows, cols):
+    codes, scales, x = inputs.make_linear(rows, cols, k, M, seed_codes=21 + k, seed_x=22 + M)
+    g = tb.Geometry(k, L, T, 1, rows, cols)
+    out = tb.matvec_axis1(to_dev_u32(codes), to_dev_f16(scales), to_dev_bf16(x), g)
+    ref, ab = oracle_mod.matvec_axis1(codes, scales, x, k, L, T)
+    check_band(oracle_mod, bf16_bits(out), ref, ab, f"axis1 k={k} M={M} {rows}x{cols}")
+
+
+def test_matvec_axis1_config_smoke_shape(oracle_mod):
+    """R=512, C=2048, k=2, M=1: the small full-check configuration."""
+    codes, scales, x = inputs.make_linear(512, 2048, 2, 1)
+    g = tb.Geometry(2, L, T, 1, 512, 2048)
+    out = tb.matvec_axis1(to_dev_u32(codes), to_dev_f16(scales), to_dev_bf16(x), g)
+    ref, ab = oracle_mod.matvec_axis1(codes, scales, x, 2, L, T)
+    check_band(oracle_mod, bf16_bits(out), ref, ab, "axis1 512x2048")
+
+
+@pytest.mark.parametrize("k", [2, 3, 4])
+def test_matvec_axis1_full_size_sampled(oracle_mod, k):
+    rows, cols, M = 17408, 5120, 4
+    codes, scales, x = inputs.make_linear(rows, cols, k, M)
+    g = tb.Geometry(k, L, T, 1, rows, cols)
+    dc, ds = to_dev_u32(codes), to_dev_f16(scales)
+    idx = _sample(rows, 40, 100 + k)
+    for m in (1, 4):
+        out = bf16_bits(tb.matvec_axis1(dc, ds, to_dev_bf16(x[:m]), g))
+        ref, ab = oracle_mod.matvec_axis1(codes, scales, x[:m], k, L, T, rows=idx)
+        check_band(oracle_mod, out[:, idx], ref, ab, f"axis1 full k={k} M={m}")
+
+
+def test_matvec_axis1_special_inputs(oracle_mod):
+    rows, cols = 64, 512
+    codes, scales, _ = inputs.make_linear(rows, cols, 2, 1)
+    g = tb.Geometry(2, L, T, 1, rows, cols)
+    dc, ds = to_dev_u32(codes), to_dev_f16(scales)
+    zero = torch.zeros((2, cols), dtype=torch.bfloat16, device="cuda")
+    assert torch.all(tb.matvec_axis1(dc, ds, zero, g) == 0)
+    e = np.zeros((1, cols), dtype=np.uint16)
+    e[0, 300] = 0x3F80
+    out = tb.matvec_axis1(dc, ds, to_dev_bf16(e), g)
+    ref, ab = oracle_mod.matvec_axis1(codes, scales, e, 2, L, T)
+    check_band(oracle_mod, bf16_bits(out), ref, ab, "one-hot")
+
+
+def test_matvec_axis1_L12(oracle_mod):
+    codes, scales, x = inputs.make_linear(50, 1024, 4, 3, seed_codes=5)
+    out = tb.matvec_axis1(to_dev_u32(codes), to_dev_f16(scales), to_dev_bf16(x), tb.Geometry(4, 12, T, 1, 50, 1024))
+    ref, ab = oracle_mod.matvec_axis1(codes, scales, x, 4, 12, T)
+    check_band(oracle_mod, bf16_bits(out), ref, ab, "axis1 L=12")
+
+
+# ------------------------------------------------------------------ gate/up
+
+def check_gateup(oracle, gpu_bits, gref, gab, uref, uab, what):
+    """Accept an output if it is within one bf16 ulp of the activation chain
+    evaluated at some pair of bf16 gate/up values that a correctly rounded
+    cast of sums inside the tolerance band can give.  Returns the fraction of
+    outputs whose gate or up band held more than one bf16 value."""
+    from util import ABS_TOL, REL_TOL, _ordered, bf16_of_f64
+    tg, tu = REL_TOL * gab + ABS_TOL, REL_TOL * uab + ABS_TOL
+    cands_g = [bf16_of_f64(oracle, gref - tg), bf16_of_f64(oracle, gref), bf16_of_f64(oracle, gref + tg)]
+    cands_u = [bf16_of_f64(oracle, uref - tu), bf16_of_f64(oracle, uref), bf16_of_f64(oracle, uref + tu)]
+    gpu = _ordered(np.asarray(gpu_bits, dtype=np.uint16))
+    ok = np.zeros(gpu.shape, dtype=bool)
+    for cg in cands_g:
+        for cu in cands_u:
+            want = _ordered(oracle.swiglu_bf16(cg, cu))
+            ok |= np.abs(gpu - want) <= 1
+    assert ok.all(), f"{what}: {int((~ok).sum())} of {ok.size} outputs off the chain"
+    multi = (cands_g[0] != cands_g[2]) | (cands_u[0] != cands_u[2])
+    return float(multi.mean())
+
+
+@pytest.mark.parametrize("k", [2, 3])
+@pytest.mark.parametrize("M", [1, 2, 3, 4])
+@pytest.mark.parametrize("rows,cols", [(33, 512), (96, 1536)])
+def test_gateup_small(oracle_mod, k, M, rows, cols):
+    gc, gs, x = inputs.make_linear(rows, cols, k, M, seed_codes=31, seed_scales=32, seed_x=33 + M)
+    uc, us, _ = inputs.make_linear(rows, cols, k, M, seed_codes=41, seed_scales=42, seed_x=43)
+    g = tb.Geometry(k, L, T, 1, rows, cols)
+    out = tb.gateup_swiglu(to_dev_u32(gc), to_dev_f16(gs), to_dev_u32(uc), to_dev_f16(us), to_dev_bf16(x), g)
+    sums = oracle_mod.gateup_sums(gc, gs, uc, us, x, k, L, T)
+    check_gateup(oracle_mod, bf16_bits(out), *sums, f"gateup k={k} M={M}")
+
+
+@pytest.mark.parametrize("k", [2, 3])
+def test_gateup_full_size_sampled(oracle_mod, k):
+    rows, cols, M = 17408, 5120, 4
+    gc, gs, x = inputs.make_linear(rows, cols, k, M, seed_codes=inputs.SEED_GATE)
+    uc, us, _ = inputs.make_linear(rows, cols, k, M, seed_codes=inputs.SEED_UP, seed_scales=inputs.SEED_SCALES + 1)
+    g = tb.Geometry(k, L, T, 1, rows, cols)
+    out = bf16_bits(tb.gateup_swiglu(to_dev_u32(gc), to_dev_f16(gs), to_dev_u32(uc), to_dev_f16(us),
+                                     to_dev_bf16(x), g))
+    idx = _sample(rows, 40, 200 + k)
+    sums = oracle_mod.gateup_sums(gc, gs, uc, us, x, k, L, T, rows=idx)
+    check_gateup(oracle_mod, out[:, idx], *sums, f"gateup full k={k}")
+
+
+# ------------------------------------------------------------------ axis 0
+
+@pytest.mark.parametrize("k", [2, 3, 4])
+@pytest.mark.parametrize("M", [1, 2, 3, 4])
+@pytest.mark.parametrize("rows,cols", [(1, 256), (77, 512), (300, 768)])
+def test_matvec_axis0_small(oracle_mod, k, M, rows, cols):
+    codes, scales, x = inputs.make_linear(rows, cols, k, M, seed_codes=51 + k, seed_x=52 + M, sigma=0.5,
+                                          x_len=rows)
+    g = tb.Geometry(k, L, T, 0, rows, cols)
+    ws = tb.new_workspace(M, g, "cuda")
+    dc, ds, dx = to_dev_u32(codes), to_dev_f16(scales), to_dev_bf16(x)
+    ref, ab = oracle_mod.matvec_axis0(codes, scales, x, k, L, T)
+    for _ in range(2):  # the workspace is reused: the second call must match too
+        out = tb.matvec_axis0(dc, ds, dx, g, ws)
+        check_band(oracle_mod, bf16_bits(out), ref, ab, f"axis0 k={k} M={M} {rows}x{cols}")
+
+
+@pytest.mark.parametrize("k", [2, 3])
+def test_matvec_axis0_full_size_sampled(oracle_mod, k):
+    rows, cols, M = 17408, 5120, 4
+    codes, scales, x = inputs.make_linear(rows, cols, k, M, sigma=0.5, x_len=rows)
+    g = tb.Geometry(k, L, T, 0, rows, cols)
+    ws = tb.new_workspace(M, g, "cuda")
+    dc, ds = to_dev_u32(codes), to_dev_f16(scales)
+    idx = _sample(cols, 40, 300 + k)
+    for m in (1, 4):
+        out = bf16_bits(tb.matvec_axis0(dc, ds, to_dev_bf16(x[:m]), g, ws))
+        ref, ab = oracle_mod.matvec_axis0(codes, scales, x[:m], k, L, T, cols=idx)
+        check_band(oracle_mod, out[:, idx], ref, ab, f"axis0 full k={k} M={m}")
+
+
+def test_matvec_axis0_is_deterministic():
+    rows, cols = 2000, 1024
+    codes, scales, x = inputs.make_linear(rows, cols, 3, 2, sigma=0.5, x_len=rows)
+    g = tb.Geometry(3, L, T, 0, rows, cols)
+    ws = tb.new_workspace(2, g, "cuda")
+    args = (to_dev_u32(codes), to_dev_f16(scales), to_dev_bf16(x), g, ws)
+    a = tb.matvec_axis0(*args).clone()
+    b = tb.matvec_axis0(*args)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))

@@ -1,0 +1,199 @@
+"""Thin ctypes binding of libtrellis.so (the C ABI in include/trellis.h).
+
+Argument marshalling only: each function checks the tensors' device, dtype,
+shape and contiguity, passes raw device pointers and the current CUDA stream
+to the C entry point of the same name, and raises on a non-zero status.  Every
+step of the computation runs in the library's CUDA kernels; there is no
+fallback -- if the library cannot be loaded, every call raises.
+
+bf16 tensors are torch.bfloat16; fp16 scales are torch.float16; codes are
+torch.int32 or torch.uint32 tensors holding the packed words.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtrellis.so")
+
+TRELLIS_OK = 0
+STATUS_NAMES = {0: "TRELLIS_OK", -1: "TRELLIS_EGEOM", -2: "TRELLIS_EM", -3: "TRELLIS_EALIGN", -4: "TRELLIS_EAXIS",
+                -5: "TRELLIS_EWORKSPACE", -6: "TRELLIS_ECUDA", -7: "TRELLIS_ENULL", -8: "TRELLIS_EDEVICE"}
+
+EXPORTS = ("trellis_abi_version", "trellis_status_string", "trellis_check_geom", "trellis_expand_bf16",
+           "trellis_matvec_axis1", "trellis_matvec_axis0", "trellis_workspace_bytes", "trellis_gateup_swiglu",
+           "trellis_gemm_prefill")
+
+
+class TrellisGeom(ctypes.Structure):
+    """Mirror of trellis_geom_t."""
+    _fields_ = [("k", ctypes.c_int32), ("L", ctypes.c_int32), ("T", ctypes.c_int32), ("axis", ctypes.c_int32),
+                ("rows", ctypes.c_int64), ("cols", ctypes.c_int64)]
+
+
+@dataclass(frozen=True)
+class Geometry:
+    """Stored-matrix geometry: k bits/weight, L-bit windows, T-long blocks."""
+    k: int
+    L: int
+    T: int
+    axis: int
+    rows: int
+    cols: int
+
+    def c(self) -> TrellisGeom:
+        return TrellisGeom(self.k, self.L, self.T, self.axis, self.rows, self.cols)
+
+    @property
+    def words_per_row(self) -> int:
+        return self.cols * self.k // 32
+
+
+class TrellisError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn}: {STATUS_NAMES.get(status, status)} ({msg})")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libtrellis.so (raises if it is missing: there is no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(f"libtrellis.so not built at {path}; run __graft_entry__.build()")
+            lib = ctypes.CDLL(path)
+            vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+            g = ctypes.POINTER(TrellisGeom)
+            lib.trellis_abi_version.restype = i32
+            lib.trellis_abi_version.argtypes = []
+            lib.trellis_status_string.restype = ctypes.c_char_p
+            lib.trellis_status_string.argtypes = [i32]
+            lib.trellis_check_geom.restype = i32
+            lib.trellis_check_geom.argtypes = [g]
+            lib.trellis_expand_bf16.restype = i32
+            lib.trellis_expand_bf16.argtypes = [vp, vp, vp, g, vp]
+            lib.trellis_matvec_axis1.restype = i32
+            lib.trellis_matvec_axis1.argtypes = [vp, vp, vp, vp, i32, g, vp]
+            lib.trellis_matvec_axis0.restype = i32
+            lib.trellis_matvec_axis0.argtypes = [vp, vp, vp, vp, i32, g, vp, sz, vp]
+            lib.trellis_workspace_bytes.restype = sz
+            lib.trellis_workspace_bytes.argtypes = [i32, g]
+            lib.trellis_gateup_swiglu.restype = i32
+            lib.trellis_gateup_swiglu.argtypes = [vp, vp, vp, vp, vp, vp, i32, g, vp]
+            lib.trellis_gemm_prefill.restype = i32
+            lib.trellis_gemm_prefill.argtypes = [vp, vp, vp, vp, i32, g, vp]
+            _lib = lib
+    return _lib
+
+
+def _check(fn: str, status: int):
+    if status != TRELLIS_OK:
+        raise TrellisError(fn, status, load().trellis_status_string(status).decode())
+
+
+def _stream(t: torch.Tensor) -> int:
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _req(t: torch.Tensor, name: str, dtypes, shape):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+_CODES = (torch.int32, getattr(torch, "uint32", torch.int32))
+
+
+def expand_bf16(codes, scales, g: Geometry, out=None):
+    """Decoded stored matrix [rows, cols] bf16 (bit-exact)."""
+    if out is None:
+        out = torch.empty((g.rows, g.cols), dtype=torch.bfloat16, device=codes.device)
+    args = (_req(codes, "codes", _CODES, (g.rows, g.words_per_row)),
+            _req(scales, "scales", (torch.float16,), (g.rows,)),
+            _req(out, "out", (torch.bfloat16,), (g.rows, g.cols)))
+    _check("trellis_expand_bf16", load().trellis_expand_bf16(*args, ctypes.byref(g.c()), _stream(codes)))
+    return out
+
+
+def matvec_axis1(codes, scales, x, g: Geometry, out=None):
+    """out[M, rows] = x[M, cols] @ W^T for an axis-1 matrix, M = 1..4."""
+    M = x.shape[0]
+    if out is None:
+        out = torch.empty((M, g.rows), dtype=torch.bfloat16, device=x.device)
+    args = (_req(codes, "codes", _CODES, (g.rows, g.words_per_row)),
+            _req(scales, "scales", (torch.float16,), (g.rows,)),
+            _req(x, "x", (torch.bfloat16,), (M, g.cols)),
+            _req(out, "out", (torch.bfloat16,), (M, g.rows)))
+    _check("trellis_matvec_axis1", load().trellis_matvec_axis1(*args, M, ctypes.byref(g.c()), _stream(x)))
+    return out
+
+
+def workspace_bytes(M: int, g: Geometry) -> int:
+    return int(load().trellis_workspace_bytes(M, ctypes.byref(g.c())))
+
+
+def new_workspace(M: int, g: Geometry, device) -> torch.Tensor:
+    """A zero-filled workspace for matvec_axis0 (reusable across calls)."""
+    n = workspace_bytes(M, g)
+    if n == 0:
+        raise ValueError("unsupported geometry or M for the axis-0 matvec")
+    return torch.zeros(((n + 15) // 16) * 4, dtype=torch.int32, device=device)
+
+
+def matvec_axis0(codes, scales, x, g: Geometry, workspace, out=None):
+    """out[M, cols] = x[M, rows] @ W^T for an axis-0 matrix (stored W^T), M = 1..4."""
+    M = x.shape[0]
+    if out is None:
+        out = torch.empty((M, g.cols), dtype=torch.bfloat16, device=x.device)
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    args = (_req(codes, "codes", _CODES, (g.rows, g.words_per_row)),
+            _req(scales, "scales", (torch.float16,), (g.rows,)),
+            _req(x, "x", (torch.bfloat16,), (M, g.rows)),
+            _req(out, "out", (torch.bfloat16,), (M, g.cols)))
+    nbytes = workspace.numel() * workspace.element_size()
+    _check("trellis_matvec_axis0", load().trellis_matvec_axis0(*args, M, ctypes.byref(g.c()), workspace.data_ptr(),
+                                                              nbytes, _stream(x)))
+    return out
+
+
+def gateup_swiglu(gcodes, gscales, ucodes, uscales, x, g: Geometry, out=None):
+    """out[M, rows] = bf16 SwiGLU chain of the gate and up matvecs, M = 1..4."""
+    M = x.shape[0]
+    if out is None:
+        out = torch.empty((M, g.rows), dtype=torch.bfloat16, device=x.device)
+    shp = (g.rows, g.words_per_row)
+    args = (_req(gcodes, "gcodes", _CODES, shp), _req(gscales, "gscales", (torch.float16,), (g.rows,)),
+            _req(ucodes, "ucodes", _CODES, shp), _req(uscales, "uscales", (torch.float16,), (g.rows,)),
+            _req(x, "x", (torch.bfloat16,), (M, g.cols)), _req(out, "out", (torch.bfloat16,), (M, g.rows)))
+    _check("trellis_gateup_swiglu", load().trellis_gateup_swiglu(*args, M, ctypes.byref(g.c()), _stream(x)))
+    return out
+
+
+def gemm_prefill(codes, scales, x, g: Geometry, out=None):
+    """out[M, rows] = x[M, cols] @ E^T with E the bf16 expand weights (tensor cores)."""
+    M = x.shape[0]
+    if out is None:
+        out = torch.empty((M, g.rows), dtype=torch.bfloat16, device=x.device)
+    args = (_req(codes, "codes", _CODES, (g.rows, g.words_per_row)),
+            _req(scales, "scales", (torch.float16,), (g.rows,)),
+            _req(x, "x", (torch.bfloat16,), (M, g.cols)),
+            _req(out, "out", (torch.bfloat16,), (M, g.rows)))
+    _check("trellis_gemm_prefill", load().trellis_gemm_prefill(*args, M, ctypes.byref(g.c()), _stream(x)))
+    return out

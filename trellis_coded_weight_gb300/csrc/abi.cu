@@ -1,0 +1,156 @@
+// abi.cu -- the exported C entry points of libtrellis.so (declared in
+// include/trellis.h): argument validation on the host, then one kernel
+// launch on the caller's stream.  Nothing here allocates device memory.
+//
+// The checks follow the pages' TrellisGeometry rules ("trellis-linear.ts":
+// trellisGeometry throws unless the words hold whole k-bit symbols and the
+// columns are whole blocks; fusedGateUpSwiglu throws for M > 4) and add the
+// GPU kernels' own supported set (k in {2,3,4}, L in {12,16}, T = 256,
+// 16-byte aligned pointers).  Every failed check returns before any CUDA call.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "launch.h"
+#include "trellis.h"
+
+namespace {
+
+constexpr int kAbiVersion = 100;
+constexpr int kMaxDevices = 64;
+// 0 = unknown, 1 = usable sm_103 device, -1 = not usable
+int g_device_ok[kMaxDevices];
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int geom_ok(const trellis_geom_t* g) {
+  if (!g) return TRELLIS_ENULL;
+  if (g->k < 2 || g->k > 4) return TRELLIS_EGEOM;
+  if (g->L != 16 && g->L != 12) return TRELLIS_EGEOM;
+  if (g->T != trellis::kT_host) return TRELLIS_EGEOM;
+  if (g->axis != 0 && g->axis != 1) return TRELLIS_EGEOM;
+  if (g->rows < 1 || g->cols < 1 || g->cols % g->T != 0) return TRELLIS_EGEOM;
+  if (((int64_t)g->T * g->k) % 32 != 0) return TRELLIS_EGEOM;
+  if (g->rows > INT32_MAX || g->cols > INT32_MAX || g->rows * g->cols > ((int64_t)1 << 40))
+    return TRELLIS_EGEOM;
+  return TRELLIS_OK;
+}
+
+// The current device must be compute capability 10.3 (the library holds
+// sm_103a code only).  Cached per device.
+int device_ok() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+    cudaGetLastError();
+    return TRELLIS_EDEVICE;
+  }
+  if (dev < kMaxDevices && g_device_ok[dev] != 0) return g_device_ok[dev] > 0 ? TRELLIS_OK : TRELLIS_EDEVICE;
+  int major = 0, minor = 0;
+  const bool ok = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+                  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
+                  major == 10 && minor == 3;
+  if (!ok) cudaGetLastError();
+  if (dev < kMaxDevices) g_device_ok[dev] = ok ? 1 : -1;
+  return ok ? TRELLIS_OK : TRELLIS_EDEVICE;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? TRELLIS_OK : TRELLIS_ECUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int trellis_abi_version(void) { return kAbiVersion; }
+
+const char* trellis_status_string(int status) {
+  switch (status) {
+    case TRELLIS_OK: return "ok";
+    case TRELLIS_EGEOM: return "unsupported or inconsistent trellis geometry";
+    case TRELLIS_EM: return "M outside the range this call supports";
+    case TRELLIS_EALIGN: return "a pointer is not 16-byte aligned";
+    case TRELLIS_EAXIS: return "the geometry's axis does not fit this call";
+    case TRELLIS_EWORKSPACE: return "workspace missing, misaligned or too small";
+    case TRELLIS_ECUDA: return "CUDA error at launch";
+    case TRELLIS_ENULL: return "a required pointer is NULL";
+    case TRELLIS_EDEVICE: return "no usable sm_103 CUDA device is current";
+    default: return "unknown status";
+  }
+}
+
+int trellis_check_geom(const trellis_geom_t* g) { return geom_ok(g); }
+
+int trellis_expand_bf16(const uint32_t* codes, const uint16_t* scales, uint16_t* out, const trellis_geom_t* g,
+                        trellis_stream_t stream) {
+  int st = geom_ok(g);
+  if (st) return st;
+  if (!codes || !scales || !out) return TRELLIS_ENULL;
+  if (!aligned16(codes) || !aligned16(scales) || !aligned16(out)) return TRELLIS_EALIGN;
+  if ((st = device_ok())) return st;
+  return cuda_status(trellis::launch_expand_bf16(codes, scales, out, g->k, g->L, g->rows, g->cols,
+                                                 static_cast<cudaStream_t>(stream)));
+}
+
+int trellis_matvec_axis1(const uint32_t* codes, const uint16_t* scales, const uint16_t* x, uint16_t* out, int M,
+                         const trellis_geom_t* g, trellis_stream_t stream) {
+  int st = geom_ok(g);
+  if (st) return st;
+  if (g->axis != 1) return TRELLIS_EAXIS;
+  if (M < 1 || M > 4) return TRELLIS_EM;
+  if (!codes || !scales || !x || !out) return TRELLIS_ENULL;
+  if (!aligned16(codes) || !aligned16(scales) || !aligned16(x) || !aligned16(out)) return TRELLIS_EALIGN;
+  if ((st = device_ok())) return st;
+  return cuda_status(trellis::launch_matvec_axis1(codes, scales, x, out, M, g->k, g->L, g->rows, g->cols,
+                                                  static_cast<cudaStream_t>(stream)));
+}
+
+size_t trellis_workspace_bytes(int M, const trellis_geom_t* g) {
+  if (geom_ok(g) != TRELLIS_OK || M < 1 || M > 4) return 0;
+  return trellis::axis0_workspace_bytes(M, g->rows, g->cols);
+}
+
+int trellis_matvec_axis0(const uint32_t* codes, const uint16_t* scales, const uint16_t* x, uint16_t* out, int M,
+                         const trellis_geom_t* g, void* workspace, size_t workspace_bytes,
+                         trellis_stream_t stream) {
+  int st = geom_ok(g);
+  if (st) return st;
+  if (g->axis != 0) return TRELLIS_EAXIS;
+  if (M < 1 || M > 4) return TRELLIS_EM;
+  if (!codes || !scales || !x || !out) return TRELLIS_ENULL;
+  if (!aligned16(codes) || !aligned16(scales) || !aligned16(x) || !aligned16(out)) return TRELLIS_EALIGN;
+  if (!workspace || !aligned16(workspace) ||
+      workspace_bytes < trellis::axis0_workspace_bytes(M, g->rows, g->cols))
+    return TRELLIS_EWORKSPACE;
+  if ((st = device_ok())) return st;
+  return cuda_status(trellis::launch_matvec_axis0(codes, scales, x, out, M, g->k, g->L, g->rows, g->cols,
+                                                  workspace, static_cast<cudaStream_t>(stream)));
+}
+
+int trellis_gateup_swiglu(const uint32_t* gcodes, const uint16_t* gscales, const uint32_t* ucodes,
+                          const uint16_t* uscales, const uint16_t* x, uint16_t* out, int M, const trellis_geom_t* g,
+                          trellis_stream_t stream) {
+  int st = geom_ok(g);
+  if (st) return st;
+  if (g->axis != 1) return TRELLIS_EAXIS;
+  if (M < 1 || M > 4) return TRELLIS_EM;
+  if (!gcodes || !gscales || !ucodes || !uscales || !x || !out) return TRELLIS_ENULL;
+  if (!aligned16(gcodes) || !aligned16(gscales) || !aligned16(ucodes) || !aligned16(uscales) || !aligned16(x) ||
+      !aligned16(out))
+    return TRELLIS_EALIGN;
+  if ((st = device_ok())) return st;
+  return cuda_status(trellis::launch_gateup_swiglu(gcodes, gscales, ucodes, uscales, x, out, M, g->k, g->L,
+                                                   g->rows, g->cols, static_cast<cudaStream_t>(stream)));
+}
+
+int trellis_gemm_prefill(const uint32_t* codes, const uint16_t* scales, const uint16_t* x, uint16_t* out, int M,
+                         const trellis_geom_t* g, trellis_stream_t stream) {
+  int st = geom_ok(g);
+  if (st) return st;
+  if (g->axis != 1) return TRELLIS_EAXIS;
+  if (M < 1 || M > (1 << 24)) return TRELLIS_EM;
+  if (!codes || !scales || !x || !out) return TRELLIS_ENULL;
+  if (!aligned16(codes) || !aligned16(scales) || !aligned16(x) || !aligned16(out)) return TRELLIS_EALIGN;
+  if ((st = device_ok())) return st;
+  return cuda_status(trellis::launch_gemm_prefill(codes, scales, x, out, M, g->k, g->L, g->rows, g->cols,
+                                                  static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,101 @@
+// common.cuh -- device primitives of the trellis (QTIP 1MAD) decode for sm_103a.
+//
+// Format and code: "trellis-linear.ts" diff page (mlx-bun 0.2.0 -> 0.4.0),
+// header comment and HEADER source (trellis_state, trellis_y, trellis_val,
+// trellis_val_rcp).  The state of position t of a T-long block is the L-bit
+// window that starts at bit (T-1-t)*k of the block (LSB-first inside
+// little-endian uint32 words, wrapping inside the block); the code of state s
+// is y = bytesum(s*34038481 + 76625530 mod 2^32) - 510.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace trellis {
+
+constexpr uint32_t kMulA = 34038481u;
+constexpr uint32_t kAddB = 76625530u;
+constexpr float kD = 147.800537109375f;
+constexpr float kRcpD = 1.0f / 147.800537109375f;  // fp32 nearest to 1/d (folded at compile time)
+constexpr int kT = 256;                             // positions per block (the only supported T)
+
+// The fp32 pattern 0x4B400000 is 1.5*2^23, whose ulp is 1: adding an integer
+// n with |n| < 2^22 to the pattern adds n to the value.  The byte-sum
+// instruction adds the four bytes onto this bias, so its result, read as a
+// float, is exactly 1.5*2^23 + y.
+constexpr uint32_t kMagicBits = 0x4B400000u;
+constexpr float kMagic = 12582912.0f;
+
+// 1MAD of a zero-extended L-bit state: bit pattern of the float 1.5*2^23 + y.
+__device__ __forceinline__ uint32_t code_magic(uint32_t s) {
+  const uint32_t x = s * kMulA + kAddB;
+  return __dp4a(x, 0x01010101u, kMagicBits - 510u);
+}
+
+// y as an exact float.
+__device__ __forceinline__ float code_y(uint32_t s) {
+  return __fsub_rn(__uint_as_float(code_magic(s)), kMagic);
+}
+
+// Correctly rounded y / d: the reciprocal product refined by one residual
+// step ("trellis_val_rcp" in the HEADER source).  The pages state, and the
+// oracle pins check exhaustively, that this equals the IEEE quotient for
+// every y in [-510, 510].
+__device__ __forceinline__ float value_rn(float y) {
+  const float q = __fmul_rn(y, kRcpD);
+  const float e = __fmaf_rn(-q, kD, y);
+  return __fmaf_rn(e, kRcpD, q);
+}
+
+// Round two floats to bf16 (nearest even) and pack them, a in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+  return r;
+}
+
+__device__ __forceinline__ float bf16lo_to_f32(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi_to_f32(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_to_f32(uint16_t v) { return __uint_as_float((uint32_t)v << 16); }
+
+__device__ __forceinline__ float f16_to_f32(uint16_t h) {
+  float f;
+  asm("{ .reg .f16 t; mov.b16 t, %1; cvt.f32.f16 %0, t; }" : "=f"(f) : "h"(h));
+  return f;
+}
+
+// The L-bit window starting at run-relative bit O of the words w[] (w[0]
+// holds run bits 0..31).  O is a compile-time constant after unrolling.
+template <int L, int NW>
+__device__ __forceinline__ uint32_t window_at(const uint32_t (&w)[NW], int O) {
+  const int wi = O >> 5, off = O & 31;
+  uint32_t v;
+  if (off == 0) v = w[wi];
+  else if (off + L <= 32) v = w[wi] >> off;
+  else v = __funnelshift_r(w[wi], w[wi + 1], off);
+  return (off + L == 32) ? v : (v & ((1u << L) - 1u));
+}
+
+// States of the 32 positions t0 .. t0+31 of a run.  Position t0+j starts at
+// run bit (31-j)*K; w[0..K] are the run's K words followed by the spill word.
+// For L = 16 and K in {2, 4}, windows 16 bits apart come from one 32-bit
+// funnel shift: the low half is one state and the high half the other.
+template <int K, int L>
+__device__ __forceinline__ void run_states(const uint32_t (&w)[K + 1], uint32_t (&s)[32]) {
+  constexpr bool kPair = (L == 16) && (K == 2 || K == 4);
+  constexpr int kPartner = 16 / K;  // j - kPartner starts 16 bits above j
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const int o = (31 - j) * K;
+    if (kPair) {
+      if ((o & 31) < 16) {
+        const uint32_t F = (o & 31) ? __funnelshift_r(w[o >> 5], w[(o >> 5) + 1], o & 31) : w[o >> 5];
+        s[j] = F & 0xFFFFu;
+        s[j - kPartner] = F >> 16;
+      }
+    } else {
+      s[j] = window_at<L, K + 1>(w, o);
+    }
+  }
+}
+
+}  // namespace trellis

@@ -1,0 +1,35 @@
+// launch.h -- internal host-side launchers of the CUDA kernels (C++ only; the
+// public C ABI is include/trellis.h).  Arguments are validated by abi.cu
+// before these are called.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace trellis {
+
+constexpr int kT_host = 256;  // positions per block, the only T the kernels support
+
+cudaError_t launch_expand_bf16(const uint32_t* codes, const uint16_t* scales, uint16_t* out, int k, int L,
+                               int64_t rows, int64_t cols, cudaStream_t st);
+
+cudaError_t launch_matvec_axis1(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
+                                uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols,
+                                cudaStream_t st);
+
+cudaError_t launch_gateup_swiglu(const uint32_t* gcodes, const uint16_t* gscales, const uint32_t* ucodes,
+                                 const uint16_t* uscales, const uint16_t* x, uint16_t* out, int M, int k,
+                                 int L, int64_t rows, int64_t cols, cudaStream_t st);
+
+// Workspace of the axis-0 matvec: fp32 partials followed by per-column-block
+// arrival counters.
+size_t axis0_workspace_bytes(int M, int64_t rows, int64_t cols);
+cudaError_t launch_matvec_axis0(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
+                                uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols,
+                                void* workspace, cudaStream_t st);
+
+cudaError_t launch_gemm_prefill(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
+                                uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols,
+                                cudaStream_t st);
+
+}  // namespace trellis
