@@ -163,6 +163,15 @@ int trellis_gateup_swiglu(const uint32_t *gcodes, const uint16_t *gscales, const
 int trellis_gemm_prefill(const uint32_t *codes, const uint16_t *scales, const uint16_t *x,
                          uint16_t *out, int M, const trellis_geom_t *g, trellis_stream_t stream);
 
+/*
+ * trellis_device_error -- diagnostic of the tensor-core kernel.  Every wait on
+ * an mbarrier inside trellis_gemm_prefill is bounded (2 s); a wait that gives
+ * up records a non-zero code in a device word instead of hanging the GPU.
+ * Returns that code (0 = none), reading it synchronously from the current
+ * device; reset != 0 clears it.  Negative values are trellis_status errors.
+ */
+int trellis_device_error(int reset);
+
 #ifdef __cplusplus
 }
 #endif

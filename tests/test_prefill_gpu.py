@@ -1,0 +1,65 @@
+"""Parity of the tcgen05 prefill GEMM against the oracle (bf16 expand weights,
+fp64 sums) and against the expand + torch.matmul comparator."""
+import numpy as np
+import pytest
+import torch
+
+from trellis_coded_weight_gb300 import binding as tb
+from trellis_coded_weight_gb300 import inputs
+from util import bf16_bits, check_band, to_dev_bf16, to_dev_f16, to_dev_u32
+
+pytestmark = pytest.mark.gpu
+L, T = 16, 256
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from trellis_coded_weight_gb300 import build
+    build.build()
+    tb.load()
+    tb.device_error(reset=True)
+    yield
+    assert tb.device_error() == 0, "a bounded wait in the prefill kernel gave up"
+
+
+@pytest.mark.parametrize("k", [2, 3, 4])
+@pytest.mark.parametrize("M,rows,cols", [(5, 128, 256), (32, 200, 768), (33, 128, 512), (100, 257, 1024),
+                                         (300, 136, 512), (64, 64, 2048)])
+def test_prefill_small(oracle_mod, k, M, rows, cols):
+    codes, scales, x = inputs.make_linear(rows, cols, k, M, seed_codes=61 + k, seed_x=62 + M)
+    g = tb.Geometry(k, L, T, 1, rows, cols)
+    out = tb.gemm_prefill(to_dev_u32(codes), to_dev_f16(scales), to_dev_bf16(x), g)
+    ref, ab = oracle_mod.prefill(codes, scales, x, k, L, T)
+    check_band(oracle_mod, bf16_bits(out), ref, ab, f"prefill k={k} M={M} {rows}x{cols}")
+
+
+@pytest.mark.parametrize("M", [32, 512, 2048])
+def test_prefill_full_size_sampled(oracle_mod, M):
+    rows, cols, k = 17408, 5120, 2
+    codes, scales, x = inputs.make_linear(rows, cols, k, M)
+    g = tb.Geometry(k, L, T, 1, rows, cols)
+    out = bf16_bits(tb.gemm_prefill(to_dev_u32(codes), to_dev_f16(scales), to_dev_bf16(x), g))
+    rng = np.random.default_rng(M)
+    idx = np.unique(np.concatenate([rng.choice(rows, 24, replace=False), [0, 127, 128, rows - 1]])).astype(np.int64)
+    ref, ab = oracle_mod.prefill(codes, scales, x, k, L, T, rows=idx)
+    check_band(oracle_mod, out[:, idx], ref, ab, f"prefill full M={M}")
+
+
+def test_prefill_matches_expand_then_matmul():
+    rows, cols, M, k = 1024, 2048, 256, 3
+    codes, scales, x = inputs.make_linear(rows, cols, k, M, seed_codes=9)
+    g = tb.Geometry(k, L, T, 1, rows, cols)
+    dc, ds, dx = to_dev_u32(codes), to_dev_f16(scales), to_dev_bf16(x)
+    w = tb.expand_bf16(dc, ds, g)
+    ref = dx.float() @ w.float().t()
+    out = tb.gemm_prefill(dc, ds, dx, g).float()
+    scale = dx.float().abs() @ w.float().abs().t()
+    assert torch.all((out - ref).abs() <= 1e-5 * scale + 1e-6 + ref.abs() * 2 ** -8)
+
+
+def test_prefill_L12(oracle_mod):
+    codes, scales, x = inputs.make_linear(130, 512, 4, 40, seed_codes=3)
+    g = tb.Geometry(4, 12, T, 1, 130, 512)
+    out = tb.gemm_prefill(to_dev_u32(codes), to_dev_f16(scales), to_dev_bf16(x), g)
+    ref, ab = oracle_mod.prefill(codes, scales, x, 4, 12, T)
+    check_band(oracle_mod, bf16_bits(out), ref, ab, "prefill L=12")

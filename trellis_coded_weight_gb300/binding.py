@@ -27,7 +27,7 @@ STATUS_NAMES = {0: "TRELLIS_OK", -1: "TRELLIS_EGEOM", -2: "TRELLIS_EM", -3: "TRE
 
 EXPORTS = ("trellis_abi_version", "trellis_status_string", "trellis_check_geom", "trellis_expand_bf16",
            "trellis_matvec_axis1", "trellis_matvec_axis0", "trellis_workspace_bytes", "trellis_gateup_swiglu",
-           "trellis_gemm_prefill")
+           "trellis_gemm_prefill", "trellis_device_error")
 
 
 class TrellisGeom(ctypes.Structure):
@@ -92,6 +92,8 @@ def load(path: str = LIB_PATH):
             lib.trellis_gateup_swiglu.argtypes = [vp, vp, vp, vp, vp, vp, i32, g, vp]
             lib.trellis_gemm_prefill.restype = i32
             lib.trellis_gemm_prefill.argtypes = [vp, vp, vp, vp, i32, g, vp]
+            lib.trellis_device_error.restype = i32
+            lib.trellis_device_error.argtypes = [i32]
             _lib = lib
     return _lib
 
@@ -197,3 +199,8 @@ def gemm_prefill(codes, scales, x, g: Geometry, out=None):
             _req(out, "out", (torch.bfloat16,), (M, g.rows)))
     _check("trellis_gemm_prefill", load().trellis_gemm_prefill(*args, M, ctypes.byref(g.c()), _stream(x)))
     return out
+
+
+def device_error(reset: bool = False) -> int:
+    """Device error word of the tensor-core kernel (0 = no bounded wait gave up)."""
+    return int(load().trellis_device_error(1 if reset else 0))

@@ -153,4 +153,11 @@ int trellis_gemm_prefill(const uint32_t* codes, const uint16_t* scales, const ui
                                                   static_cast<cudaStream_t>(stream)));
 }
 
+int trellis_device_error(int reset) {
+  int st = device_ok();
+  if (st) return st;
+  const int v = trellis::read_device_error(reset);
+  return v < 0 ? TRELLIS_ECUDA : v;
+}
+
 }  // extern "C"

@@ -32,4 +32,7 @@ cudaError_t launch_gemm_prefill(const uint32_t* codes, const uint16_t* scales, c
                                 uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols,
                                 cudaStream_t st);
 
+// Device error word of the tensor-core kernels (bounded waits that gave up).
+int read_device_error(int reset);
+
 }  // namespace trellis
