@@ -253,3 +253,226 @@ def run_gpu(args):
         tdist.barrier()
         tdist.destroy_process_group()
     return res
+
+
+def run_prefill(args, dev, stream, tb, inputs):
+    """Prefill GEMM R=17408 C=5120 k=2 M=2048 (tcgen05) and the expand + cuBLAS comparator."""
+    import torch
+    k, M = 2, PREFILL_M
+    g = tb.Geometry(k, L, T, 1, R, C)
+    sets = [(_dev_words(inputs.random_words(inputs.SEED_CODES + 5000 + i, (R, C * k // 32)), dev),
+             _dev_bf16(inputs.normal_bf16(inputs.SEED_X + 5000 + i, (M, C)), dev)) for i in range(3)]
+    sc = _dev_f16(inputs.uniform_f16(inputs.SEED_SCALES, (R,)), dev)
+    out = torch.empty((M, R), dtype=torch.bfloat16, device=dev)
+    wtmp = torch.empty((R, C), dtype=torch.bfloat16, device=dev)
+    n = max(3, args.steps)
+
+    def timed(fn):
+        for i in range(3):
+            fn(i % 3)
+        torch.cuda.synchronize(dev)
+        es = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        for i in range(n):
+            es[i][0].record(stream)
+            fn(i % 3)
+            es[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        return statistics.median(a.elapsed_time(b) for a, b in es)
+
+    ms = timed(lambda i: tb.gemm_prefill(sets[i][0], sc, sets[i][1], g, out))
+    ms_cmp = timed(lambda i: torch.matmul(sets[i][1], tb.expand_bf16(sets[i][0], sc, g, wtmp).t()))
+    flops = 2.0 * M * R * C
+    return {"M": M, "k": k, "rows": R, "cols": C, "ms": ms, "tflops": flops / (ms * 1e-3) / 1e12,
+            "comparator": {"what": "trellis_expand_bf16 + torch.matmul (cuBLAS)", "ms": ms_cmp,
+                           "tflops": flops / (ms_cmp * 1e-3) / 1e12}}
+
+
+def run_extra(args, dev, stream, tb, inputs, l2):
+    """Other hot-path rows at their full sizes (informational; printed to stderr)."""
+    import torch
+    res = []
+    n = max(5, args.steps)
+
+    def timed(fn, nrot):
+        for i in range(3):
+            fn(i % nrot)
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(n):
+            fn(i % nrot)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / n
+
+    for kind, ks in (("gateup", (2, 3)), ("axis0", (2, 3)), ("expand", (2, 3, 4))):
+        for k in ks:
+            per = packed_bytes(k) * (2 if kind == "gateup" else 1)
+            nrot = int(2 * l2 // per) + 2
+            cs = [_dev_words(inputs.random_words(9000 + 37 * i + k, (R, C * k // 32)), dev)
+                  for i in range(nrot * (2 if kind == "gateup" else 1))]
+            sc = _dev_f16(inputs.uniform_f16(inputs.SEED_SCALES, (R,)), dev)
+            g = tb.Geometry(k, L, T, 0 if kind == "axis0" else 1, R, C)
+            for M in ((1,) if kind == "expand" else MS):
+                if kind == "gateup":
+                    x = _dev_bf16(inputs.normal_bf16(inputs.SEED_X, (M, C)), dev)
+                    o = torch.empty((M, R), dtype=torch.bfloat16, device=dev)
+                    fn = lambda i: tb.gateup_swiglu(cs[2 * i], sc, cs[2 * i + 1], sc, x, g, o)
+                elif kind == "axis0":
+                    x = _dev_bf16(inputs.normal_bf16(inputs.SEED_X, (M, R), 0.5), dev)
+                    o = torch.empty((M, C), dtype=torch.bfloat16, device=dev)
+                    ws = tb.new_workspace(M, g, dev)
+                    fn = lambda i: tb.matvec_axis0(cs[i], sc, x, g, ws, o)
+                else:
+                    o = torch.empty((R, C), dtype=torch.bfloat16, device=dev)
+                    fn = lambda i: tb.expand_bf16(cs[i], sc, g, o)
+                ms = timed(fn, nrot)
+                row = {"kind": kind, "k": k, "M": M, "us": ms * 1e3, "packed_GBps": per / (ms * 1e-3) / 1e9}
+                if kind == "expand":
+                    row["bytes_GBps"] = (per + R * C * 2) / (ms * 1e-3) / 1e9
+                res.append(row)
+            del cs
+    return res
+
+
+def cpu_baseline(seconds: float = 12.0):
+    """The oracle as it stands (one host core) on a bounded sample of rows of
+    the same twelve (k, M) launches; GB/s of the sampled rows' packed bytes."""
+    import oracle
+    from trellis_coded_weight_gb300 import inputs
+    oracle.build()
+    data = {k: inputs.make_linear(R, C, k, 4, seed_codes=inputs.SEED_CODES + k) for k in KS}
+    rows_per = 8
+    t = time.perf_counter()
+    for k in KS:  # calibrate on a tiny sample
+        oracle.matvec_axis1(data[k][0], data[k][1], data[k][2][:1], k, L, T, rows=np.arange(rows_per))
+    per_row = (time.perf_counter() - t) / (rows_per * len(KS))
+    n = max(8, int(seconds / (per_row * len(KS) * len(MS))))
+    n = min(n, R)
+    rng = np.random.default_rng(1)
+    idx = np.sort(rng.choice(R, n, replace=False)).astype(np.int64)
+    nbytes = 0
+    t = time.perf_counter()
+    for k in KS:
+        for M in MS:
+            oracle.matvec_axis1(data[k][0], data[k][1], data[k][2][:M], k, L, T, rows=idx)
+            nbytes += n * C * k // 8
+    dt = time.perf_counter() - t
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} random rows (of {R}) of each of the 12 (k, M) matvecs, {dt:.1f} s on one core"}
+
+
+def run_reference(args):
+    """Reference arm: the oracle, timed on host cores, same metric and config."""
+    import oracle
+    from trellis_coded_weight_gb300 import inputs
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    oracle.build()
+    data = {k: inputs.make_linear(R, C, k, 4, seed_codes=inputs.SEED_CODES + k) for k in KS}
+    rows = 96  # rows per launch: one step is about 0.5 s of one core
+    idx = np.arange(rows, dtype=np.int64)
+
+    def step():
+        for k in KS:
+            for M in MS:
+                oracle.matvec_axis1(data[k][0], data[k][1], data[k][2][:M], k, L, T, rows=idx)
+
+    for _ in range(args.warmup):
+        step()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t
+    nbytes = sum(rows * C * k // 8 for k in KS for M in MS) * args.steps
+    v = nbytes / dt / 1e9
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded SplitMix64)", "config": workload_desc(),
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{rows} rows (of {R}) of each of the 12 (k, M) matvecs per step"},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def kernel_source_hash(name: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in (name, "common.cuh"):
+        with open(os.path.join(ROOT, "trellis_coded_weight_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel_file: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel's source changed since the capture."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            d = json.load(f).get(kernel_file)
+        if d and d.get("source_hash") == kernel_source_hash(kernel_file):
+            return d
+    except Exception:
+        pass
+    return None
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--extra", action="store_true", help="also time gate/up, axis-0 and expand (stderr)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    if args.impl == "reference":
+        res = run_reference(args)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+
+    res = run_gpu(args)
+    if res["rank"] != 0:
+        return
+    peaks, peak_src = load_peaks()
+    world = res["world"]
+    per = res["per_launch"]
+    # roofline of the dominant kernel (the axis-1 matvec; every timed launch is one)
+    alg = {(k, M): packed_bytes(k) + 2 * R + 2 * M * C + 2 * M * R for k in KS for M in MS}
+    achieved = sum(alg.values()) / (sum(per.values()) * 1e-3) / 1e9
+    hbm = float(peaks["hbm_gbs"])
+    traffic = measured_traffic("matvec_axis1.cu")
+    roofline = {"kernel": "mv1_kernel (trellis_matvec_axis1)", "bound": "hbm", "achieved": achieved, "peak": hbm,
+                "unit": "GB/s", "frac": achieved / hbm, "peak_source": f"{peak_src} hbm_gbs",
+                "traffic": (traffic["dram_bytes_per_launch"] if traffic else None),
+                "algorithmic_bytes_per_launch": sum(alg.values()) / len(alg)}
+    breakdown = [{"k": k, "M": M, "us": per[(k, M)] * 1e3,
+                  "packed_GBps": packed_bytes(k) / (per[(k, M)] * 1e-3) / 1e9,
+                  "frac_hbm": packed_bytes(k) / (per[(k, M)] * 1e-3) / 1e9 / hbm} for k in KS for M in MS]
+    pf = res["prefill"]
+    pf["frac"] = pf["tflops"] / float(peaks["bf16_tflops"])
+    pf["peak"] = float(peaks["bf16_tflops"])
+    pf["peak_source"] = f"{peak_src} bf16_tflops (burst)"
+    line = {
+        "metric": METRIC, "value": res["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": res["ms_total"] / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic: seeded SplitMix64 code words, fp16 scales U[0.005,0.02], bf16 x ~ N(0,1)",
+        "config": workload_desc(), "frac_hbm": res["value"] / world / hbm,
+        "roofline": roofline, "e2e": res["e2e"], "gpu_launches": res["launches"], "clocks": res["clocks"],
+        "prefill": pf, "breakdown": breakdown,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    if "extra" in res:
+        print(json.dumps({"extra": res["extra"]}), file=sys.stderr, flush=True)
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()
