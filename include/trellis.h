@@ -131,6 +131,34 @@ int trellis_matvec_axis0(const uint32_t *codes, const uint16_t *scales, const ui
 size_t trellis_workspace_bytes(int M, const trellis_geom_t *g);
 
 /*
+ * trellis_matvec_axis0_noalloc -- the same axis-0 matvec as
+ * trellis_matvec_axis0, for callers that cannot allocate device memory: a
+ * custom-operator slot in an inference engine that passes a kernel only its
+ * input and output tensors, or a serving runtime that plans all device
+ * memory before it starts and forbids cudaMalloc afterwards.  The pages have
+ * no counterpart; this call is an addition of this library.
+ *
+ * It takes no workspace argument.  The split-row partial sums live in a
+ * fixed array of TRELLIS_NOALLOC_SCRATCH_BYTES bytes of device memory that
+ * the library defines; every GPU that loads the library holds that array
+ * until the process exits.  The call allocates nothing: it clears the
+ * array's arrival counters with cudaMemsetAsync on `stream` and launches the
+ * axis-0 kernel.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress, with that device current) and caches it;
+ * make that first call before any stream capture.  All calls share the one
+ * array, so calls whose executions overlap on the GPU race: issue them on
+ * one stream or otherwise serialise them.
+ *
+ * Arguments, shapes and results are those of trellis_matvec_axis0.  Returns
+ * TRELLIS_EWORKSPACE when trellis_workspace_bytes(M, g) exceeds
+ * TRELLIS_NOALLOC_SCRATCH_BYTES (the problem needs more scratch than the
+ * fixed array holds; use trellis_matvec_axis0 with a larger workspace).
+ */
+#define TRELLIS_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20) /* 4 MiB */
+int trellis_matvec_axis0_noalloc(const uint32_t *codes, const uint16_t *scales, const uint16_t *x,
+                                 uint16_t *out, int M, const trellis_geom_t *g, trellis_stream_t stream);
+
+/*
  * trellis_gateup_swiglu -- fused gate/up projections with the SwiGLU
  * activation for M = 1..4 ("trellis-linear.ts": fusedGateUpSwiglu /
  * GATEUP_SOURCE; "trellis-shared-m.ts": GATEUP_SHARED_M_SOURCE).  Both
