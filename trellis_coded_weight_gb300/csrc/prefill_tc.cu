@@ -8,19 +8,26 @@
 // -- the expand numerics -- with fp32 accumulation.  The pages decode each
 // weight tile into threadgroup memory and run 8x8 SIMD-group MMAs.
 //
-// GB300 design (one CTA per 128-row x BN-token output tile):
-//   warp 0     TMA producer: x tiles [BN tokens][64 columns] land in shared
-//              memory in the 128-byte swizzled K-major layout.
-//   warp 1     allocates BN tensor-memory columns; one lane issues
-//              tcgen05.mma (M=128, N=BN, K=16, bf16 -> fp32 in TMEM) four times
-//              per 64-column stage and commits each stage back to the ring.
-//   warps 2-9  decoders: each thread decodes a run of 32 positions of one of
-//              the tile's 128 weight rows straight into the swizzled A tile
-//              (generic-proxy stores, then fence.proxy.async), then, after the
-//              last stage, the epilogue: tcgen05.ld of the accumulator,
-//              bf16 conversion, a transpose through shared memory, and
-//              coalesced 16-byte stores of out[m][r].
-// A ring of NS stages (A 16 KB + B BN*128 bytes each) decouples the three.
+// GB300 design: a persistent kernel, one CTA per SM, walking output tiles of
+// 128 weight rows x BN tokens (tile t -> row tile t % nRT, token tile t / nRT,
+// so the CTAs running together share one token tile of x in L2).
+//   warp 0      TMA producer: x tiles [BN tokens][64 columns] land in shared
+//               memory in the 128-byte swizzled K-major layout.
+//   warp 1      allocates 2*BN tensor-memory columns (two accumulators); one
+//               lane issues tcgen05.mma (M=128, N=BN, K=16, bf16 -> fp32)
+//               four times per 64-column stage and commits each stage back to
+//               the ring and each finished tile to the epilogue.
+//   warps 2-5   epilogue: tcgen05.ld of a finished accumulator (each warp
+//               reads its own 32-lane sub-partition), bf16 conversion and
+//               coalesced stores of out[m][r]; the accumulator is released
+//               while the MMA already fills the other one.
+//   warps 6-21  decoders in two groups of eight, taking alternate stages:
+//               each thread decodes a run of 32 positions of one of the
+//               tile's 128 weight rows straight into the swizzled A tile
+//               (generic-proxy stores, then fence.proxy.async).  The code
+//               words of a run are loaded two stages ahead.
+// A ring of NS stages (A 16 KB + B BN*128 bytes each) decouples producer,
+// decoders and MMA; every mbarrier wait is bounded.
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -41,8 +48,9 @@ namespace {
 constexpr int kBM = 128;               // weight rows per tile (MMA M)
 constexpr int kBK = 64;                // columns per stage (one 128-byte swizzle row of bf16)
 constexpr int kATile = kBM * kBK * 2;  // 16 KB
-constexpr int kProdWarp = 0, kMmaWarp = 1, kDecWarp0 = 2, kDecWarps = 8;
-constexpr int kThreads = 32 * (kDecWarp0 + kDecWarps);
+constexpr int kProdWarp = 0, kMmaWarp = 1, kEpiWarp0 = 2, kEpiWarps = 4, kDecWarp0 = 6;
+constexpr int kGroupWarps = 8, kGroups = 2;
+constexpr int kThreads = 32 * (kDecWarp0 + kGroups * kGroupWarps);  // 704
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
 
 struct PrefillParams {
@@ -51,6 +59,7 @@ struct PrefillParams {
   uint16_t* out;
   int64_t R, C;
   int M, nb;
+  int nRT, nTiles;  // row tiles, total tiles
 };
 
 template <int BN>
@@ -58,25 +67,37 @@ struct Cfg {
   static constexpr int NS = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);  // ring stages
   static constexpr int BTile = BN * kBK * 2;
   static constexpr int Stage = kATile + BTile;
-  static constexpr int TmemCols = BN < 32 ? 32 : BN;
+  static constexpr int TmemCols = 2 * BN < 32 ? 32 : 2 * BN;  // two accumulators
   static constexpr size_t Smem = 1024 + (size_t)NS * Stage + 256;
 };
 
-// Decode 32 consecutive positions (one run) of weight row rl of the tile into
-// the A tile: bf16(value*scale) in the 128-byte swizzled K-major layout, where
-// 16-byte chunk q of row rl sits at chunk position q ^ (rl & 7).
-template <int K, int L>
-__device__ __forceinline__ void decode_run_to_tile(const uint32_t* __restrict__ blk, int q, float scale,
-                                                   uint8_t* a_tile, int rl, int chunk0) {
-  constexpr int WPB = kT * K / 32;
+// The words of one run (K words of positions 32q .. 32q+31 plus the spill
+// word, which wraps to word 0 for the block's last run).
+template <int K>
+struct RunWords {
   uint32_t w[K + 1];
+  float scale;
+};
+
+template <int K>
+__device__ __forceinline__ void load_run(RunWords<K>& rw, const uint32_t* __restrict__ blk, int q,
+                                         const uint16_t* __restrict__ sc) {
+  constexpr int WPB = kT * K / 32;
 #pragma unroll
-  for (int i = 0; i < K; ++i) w[i] = __ldg(blk + (7 - q) * K + i);
-  w[K] = __ldg(blk + ((8 - q) * K) % WPB);
+  for (int i = 0; i < K; ++i) rw.w[i] = __ldg(blk + (7 - q) * K + i);
+  rw.w[K] = __ldg(blk + ((8 - q) * K) % WPB);
+  rw.scale = f16_to_f32(__ldg(sc));
+}
+
+// Decode one run into the A tile: bf16(value*scale) in the 128-byte swizzled
+// K-major layout, where 16-byte chunk q of row rl sits at chunk q ^ (rl & 7).
+template <int K, int L>
+__device__ __forceinline__ void decode_run_to_tile(const RunWords<K>& rw, uint8_t* a_tile, int rl, int chunk0) {
   uint32_t s[32];
-  run_states<K, L>(w, s);
+  run_states<K, L>(rw.w, s);
   const float2 nmagic = make_float2(-kMagic, -kMagic);
-  const float2 rcp = make_float2(kRcpD, kRcpD), nd = make_float2(-kD, -kD), sc = make_float2(scale, scale);
+  const float2 rcp = make_float2(kRcpD, kRcpD), nd = make_float2(-kD, -kD);
+  const float2 sc = make_float2(rw.scale, rw.scale);
   uint32_t packed[16];
 #pragma unroll
   for (int j = 0; j < 32; j += 2) {
@@ -113,26 +134,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* a_tiles = smem;                          // NS x 16 KB
   uint8_t* b_tiles = smem + (size_t)NS * kATile;    // NS x BN*128 B
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)NS * C_::Stage);
-  uint64_t* full_a = bars;           // decoders -> MMA (8 warp arrivals)
-  uint64_t* full_b = bars + NS;      // TMA -> MMA (1 arrival + tx bytes)
-  uint64_t* empty = bars + 2 * NS;   // MMA commit -> producer and decoders
-  uint64_t* acc_full = bars + 3 * NS;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * NS + 1);
-  int* fail = reinterpret_cast<int*>(tmem_slot + 1);
+  uint64_t* full_a = bars;             // decoder group -> MMA (8 warp arrivals)
+  uint64_t* full_b = bars + NS;        // TMA -> MMA (1 arrival + tx bytes)
+  uint64_t* empty = bars + 2 * NS;     // MMA commit -> producer and decoders
+  uint64_t* acc_full = bars + 3 * NS;  // [2] MMA commit -> epilogue
+  uint64_t* acc_empty = bars + 3 * NS + 2;  // [2] epilogue warps -> MMA
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * NS + 4);
+  volatile int* fail = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t r0 = (int64_t)blockIdx.x * kBM;
-  const int m0 = blockIdx.y * BN;
+  const int G = gridDim.x;
+  const int n_local = (p.nTiles - (int)blockIdx.x + G - 1) / G;
   const int nk = (int)(p.C / kBK);
-  const uint64_t deadline = tc::globaltimer() + kWaitNs;
+  const int64_t total = (int64_t)n_local * nk;  // stages this CTA runs
+  const uint64_t deadline = kWaitNs;  // per wait
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
-      tc::mbar_init(full_a + s, kDecWarps);
+      tc::mbar_init(full_a + s, kGroupWarps);
       tc::mbar_init(full_b + s, 1);
       tc::mbar_init(empty + s, 1);
     }
-    tc::mbar_init(acc_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(acc_full + b, 1);
+      tc::mbar_init(acc_empty + b, kEpiWarps);
+    }
     *fail = 0;
     tc::fence_mbar_init();
   }
@@ -144,100 +170,126 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  const uint32_t tmem_d = *tmem_slot;
+  const uint32_t tmem = *tmem_slot;
 
   if (warp == kProdWarp) {
     if (lane == 0) {
-      int issued = 0;
-      for (int ks = 0; ks < nk; ++ks) {
-        const int s = ks % NS;
-        if (ks >= NS && !tc::mbar_wait(empty + s, ((ks / NS) & 1) ^ 1, deadline)) { *fail = 1; break; }
-        tc::mbar_arrive_expect_tx(full_b + s, (uint32_t)C_::BTile);
-        tc::tma_load_2d(b_tiles + (size_t)s * C_::BTile, &tmap_x, full_b + s, ks * kBK, m0);
-        ++issued;
+      int64_t g = 0;
+      int64_t issued = 0;
+      for (int lt = 0; lt < n_local && !*fail; ++lt) {
+        const int t = (int)blockIdx.x + lt * G;
+        const int m0 = (t / p.nRT) * BN;
+        for (int ks = 0; ks < nk; ++ks, ++g) {
+          const int s = (int)(g % NS);
+          if (g >= NS && !tc::mbar_wait(empty + s, (uint32_t)((g / NS) & 1) ^ 1u, deadline)) { *fail = 1; break; }
+          tc::mbar_arrive_expect_tx(full_b + s, (uint32_t)C_::BTile);
+          tc::tma_load_2d(b_tiles + (size_t)s * C_::BTile, &tmap_x, full_b + s, ks * kBK, m0);
+          ++issued;
+        }
       }
       if (*fail) {  // let copies already in flight land before the CTA exits
-        for (int ks = (issued > NS ? issued - NS : 0); ks < issued; ++ks)
-          tc::mbar_wait(full_b + ks % NS, (ks / NS) & 1, tc::globaltimer() + kWaitNs);
+        for (int64_t j = (issued > NS ? issued - NS : 0); j < issued; ++j)
+          tc::mbar_wait(full_b + j % NS, (uint32_t)((j / NS) & 1), kWaitNs);
       }
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       const uint32_t a0 = tc::smem_u32(a_tiles), b0 = tc::smem_u32(b_tiles);
-      for (int ks = 0; ks < nk; ++ks) {
-        const int s = ks % NS;
-        const uint32_t ph = (ks / NS) & 1;
-        if (!tc::mbar_wait(full_a + s, ph, deadline) || !tc::mbar_wait(full_b + s, ph, deadline)) {
+      int64_t g = 0;
+      for (int lt = 0; lt < n_local && !*fail; ++lt) {
+        const int buf = lt & 1;
+        if (lt >= 2 && !tc::mbar_wait(acc_empty + buf, (uint32_t)((lt >> 1) & 1) ^ 1u, deadline)) {
           *fail = 1;
           break;
         }
         tc::fence_after_sync();
-        const uint64_t ad = tc::desc_sw128(a0 + s * kATile), bd = tc::desc_sw128(b0 + s * C_::BTile);
+        const uint32_t d = tmem + (uint32_t)(buf * BN);
+        for (int ks = 0; ks < nk; ++ks, ++g) {
+          const int s = (int)(g % NS);
+          const uint32_t ph = (uint32_t)((g / NS) & 1);
+          if (!tc::mbar_wait(full_a + s, ph, deadline) || !tc::mbar_wait(full_b + s, ph, deadline)) {
+            *fail = 1;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint64_t ad = tc::desc_sw128(a0 + s * kATile), bd = tc::desc_sw128(b0 + s * C_::BTile);
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk)  // +32 bytes along K per MMA: +2 in the address field
-          tc::mma_bf16(tmem_d, ad + 2 * kk, bd + 2 * kk, kIdesc, (ks | kk) != 0 ? 1u : 0u);
-        tc::mma_commit(empty + s);
+          for (int kk = 0; kk < kBK / 16; ++kk)  // +32 bytes along K per MMA: +2 in the address field
+            tc::mma_bf16(d, ad + 2 * kk, bd + 2 * kk, kIdesc, (ks | kk) != 0 ? 1u : 0u);
+          tc::mma_commit(empty + s);
+        }
+        tc::mma_commit(acc_full + buf);
       }
-      tc::mma_commit(acc_full);
+    }
+  } else if (warp < kEpiWarp0 + kEpiWarps) {
+    // ---------------- epilogue ----------------
+    const int sp = warp & 3;  // TMEM sub-partition this warp may read
+    for (int lt = 0; lt < n_local; ++lt) {
+      const int buf = lt & 1;
+      const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(acc_full + buf, (uint32_t)((lt >> 1) & 1), deadline));
+      tc::fence_after_sync();
+      if (!ok) { *fail = 1; break; }
+      const int t = (int)blockIdx.x + lt * G;
+      const int64_t row = (int64_t)(t % p.nRT) * kBM + 32 * sp + lane;
+      const int m0 = (t / p.nRT) * BN;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t v[32];
+        tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * sp) << 16) + (uint32_t)(buf * BN + c0), v);
+        tc::tmem_ld_wait();
+        if (row < p.R) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int m = m0 + c0 + i;
+            if (m < p.M) {
+              uint16_t o;
+              asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(o) : "f"(__uint_as_float(v[i])));
+              p.out[(int64_t)m * p.R + row] = o;
+            }
+          }
+        }
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(acc_empty + buf);
     }
   } else {
     // ---------------- decoders ----------------
-    const int dw = warp - kDecWarp0;           // 0..7
-    const int rl = (dw & 3) * 32 + lane;       // tile row of this thread
-    const int h = dw >> 2;                     // which 32-column half of a stage
-    const int64_t r = (r0 + rl < p.R) ? r0 + rl : p.R - 1;  // rows past the end decode row R-1, never stored
-    const float scale = f16_to_f32(__ldg(p.scales + r));
-    const uint32_t* crow = p.codes + r * (int64_t)p.nb * WPB;
-    for (int ks = 0; ks < nk; ++ks) {
-      const int s = ks % NS;
-      if (ks >= NS && !tc::mbar_wait(empty + s, ((ks / NS) & 1) ^ 1, deadline)) { *fail = 1; break; }
-      const int b = ks >> 2, q = 2 * (ks & 3) + h;  // block and run inside it
-      decode_run_to_tile<K, L>(crow + (int64_t)b * WPB, q, scale, a_tiles + (size_t)s * kATile, rl, 4 * h);
+    const int dw = warp - kDecWarp0;       // 0..15
+    const int grp = dw / kGroupWarps;      // stages g with g % 2 == grp
+    const int gw = dw % kGroupWarps;
+    const int rl = (gw & 3) * 32 + lane;   // tile row of this thread
+    const int h = gw >> 2;                 // which 32-column half of a stage
+    auto fetch = [&](RunWords<K>& rw, int64_t g) {
+      if (g >= total) return;
+      const int lt = (int)(g / nk), ks = (int)(g % nk);
+      const int t = (int)blockIdx.x + lt * G;
+      int64_t r = (int64_t)(t % p.nRT) * kBM + rl;
+      if (r >= p.R) r = p.R - 1;  // rows past the end decode row R-1 and are never stored
+      const uint32_t* blk = p.codes + (r * p.nb + (ks >> 2)) * WPB;
+      load_run<K>(rw, blk, 2 * (ks & 3) + h, p.scales + r);
+    };
+    auto process = [&](const RunWords<K>& rw, int64_t g) -> bool {
+      const int s = (int)(g % NS);
+      if (g >= NS && !tc::mbar_wait(empty + s, (uint32_t)((g / NS) & 1) ^ 1u, deadline)) return false;
+      decode_run_to_tile<K, L>(rw, a_tiles + (size_t)s * kATile, rl, 4 * h);
       tc::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(full_a + s);
-    }
-
-    // ---------------- epilogue ----------------
-    const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(acc_full, 0, deadline));
-    tc::fence_after_sync();
-    if (!ok) *fail = 1;
-    const int sp = warp & 3;                  // TMEM sub-partition this warp may read
-    const int ch = dw >> 2;                   // which of the two warps on this sub-partition
-    uint16_t* stg = reinterpret_cast<uint16_t*>(smem);  // [BN][128] bf16, reuses the ring
-    if (ok) {
-#pragma unroll 1
-      for (int cc = ch; cc < BN / 32; cc += 2) {  // 32-column chunks alternate between the two warps
-        const int c0 = cc * 32;
-        uint32_t v[32];
-        tc::tmem_ld_32x32b_x32(tmem_d + ((uint32_t)(32 * sp) << 16) + (uint32_t)c0, v);
-        tc::tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          uint16_t o;
-          asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(o) : "f"(__uint_as_float(v[i])));
-          stg[(c0 + i) * kBM + 32 * sp + lane] = o;
-        }
-      }
-    }
-    tc::fence_before_sync();
-    asm volatile("bar.sync 1, %0;" ::"r"(32 * kDecWarps) : "memory");
-    if (ok) {
-      const int t = threadIdx.x - 32 * kDecWarp0;  // 0..255
-      const bool vec = (p.R % 8) == 0;
-      for (int id = t; id < BN * 16; id += 32 * kDecWarps) {
-        const int tok = id >> 4, cc = id & 15;
-        const int m = m0 + tok;
-        const int64_t rr = r0 + cc * 8;
-        if (m >= p.M || rr >= p.R) continue;
-        const uint16_t* src = stg + tok * kBM + cc * 8;
-        uint16_t* dst = p.out + (int64_t)m * p.R + rr;
-        if (vec && rr + 8 <= p.R) {
-          *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
-        } else {
-          for (int i = 0; i < 8 && rr + i < p.R; ++i) dst[i] = src[i];
-        }
-      }
+      return true;
+    };
+    RunWords<K> ra, rb;
+    int64_t g = grp;
+    fetch(ra, g);
+    fetch(rb, g + 2);
+    while (g < total) {
+      if (!process(ra, g)) { *fail = 1; break; }
+      fetch(ra, g + 4);
+      g += 2;
+      if (g >= total) break;
+      if (!process(rb, g)) { *fail = 1; break; }
+      fetch(rb, g + 4);
+      g += 2;
     }
   }
 
@@ -246,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && *fail) report(1);
   if (warp == kMmaWarp) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem_d, C_::TmemCols);
+    tc::tmem_dealloc(tmem, C_::TmemCols);
   }
 }
 
@@ -263,8 +315,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 148;
+  return n;
+}
+
 template <int K, int L, int BN>
-cudaError_t prefill_launch(const PrefillParams& p, const uint16_t* x, cudaStream_t st) {
+cudaError_t prefill_launch(PrefillParams p, const uint16_t* x, cudaStream_t st) {
   auto fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
   CUtensorMap map;
@@ -284,7 +343,10 @@ cudaError_t prefill_launch(const PrefillParams& p, const uint16_t* x, cudaStream
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const dim3 grid((unsigned)((p.R + kBM - 1) / kBM), (unsigned)((p.M + BN - 1) / BN));
+  p.nRT = (int)((p.R + kBM - 1) / kBM);
+  p.nTiles = p.nRT * ((p.M + BN - 1) / BN);
+  const int sms = sm_count();
+  const int grid = p.nTiles < sms ? p.nTiles : sms;
   kern<<<grid, kThreads, Cfg<BN>::Smem, st>>>(map, p);
   return cudaGetLastError();
 }

@@ -51,9 +51,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase of the given parity; false once the deadline (ns of
-// %globaltimer) has passed.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t deadline) {
+// Wait for the phase of the given parity; false once timeout_ns (of
+// %globaltimer) have passed since the first unsuccessful try.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t deadline = globaltimer() + timeout_ns;
   for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 63u && globaltimer() > deadline) return false;
