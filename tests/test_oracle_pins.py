@@ -183,3 +183,18 @@ def test_geometry_rules(oracle_mod):
     assert oracle_mod.geom_check(3, 16, 16, 4, 512) != 0    # T*k not whole words
     assert oracle_mod.geom_check(2, 0, 256, 4, 512) != 0
     assert oracle_mod.geom_check(2, 16, 256, 0, 512) != 0
+
+
+def test_split_reciprocal_is_correctly_rounded():
+    """y/d as fma(y, r_hi, y * r_lo), with r_hi the fp32 nearest to 1/d and
+    r_lo the fp32 nearest to (1/d in double) - r_hi, is the correctly rounded
+    quotient for every reachable y (the value step of trellis_val).  Exact
+    rational arithmetic; the constants are formed as a C++ compiler forms them."""
+    dq = Fraction(D)
+    r_hi = np.float32(1.0) / np.float32(D)
+    r_lo = np.float32(1.0 / D - float(r_hi))
+    assert r_hi == _round_f32(1 / dq)
+    for y in range(-510, 511):
+        t = _round_f32(Fraction(y) * Fraction(float(r_lo)))
+        v = _round_f32(Fraction(y) * Fraction(float(r_hi)) + Fraction(float(t)))
+        assert v == _round_f32(Fraction(y) / dq), y

@@ -24,7 +24,7 @@ def _lib():
 
 @pytest.mark.parametrize("k", [2, 3, 4])
 @pytest.mark.parametrize("M,rows,cols", [(5, 128, 256), (32, 200, 768), (33, 128, 512), (100, 257, 1024),
-                                         (300, 136, 512), (64, 64, 2048)])
+                                         (300, 136, 512), (64, 64, 2048), (600, 130, 1024)])
 def test_prefill_small(oracle_mod, k, M, rows, cols):
     codes, scales, x = inputs.make_linear(rows, cols, k, M, seed_codes=61 + k, seed_x=62 + M)
     g = tb.Geometry(k, L, T, 1, rows, cols)

@@ -11,23 +11,26 @@
 // GB300 design: a persistent kernel, one CTA per SM, walking output tiles of
 // 128 weight rows x BN tokens (tile t -> row tile t % nRT, token tile t / nRT,
 // so the CTAs running together share one token tile of x in L2).
-//   warp 0      TMA producer: x tiles [BN tokens][64 columns] land in shared
-//               memory in the 128-byte swizzled K-major layout.
-//   warp 1      allocates 2*BN tensor-memory columns (two accumulators); one
-//               lane issues tcgen05.mma (M=128, N=BN, K=16, bf16 -> fp32)
-//               four times per 64-column stage and commits each stage back to
-//               the ring and each finished tile to the epilogue.
+//   warp 0      TMA producer: x tiles [BN tokens][BK columns] land in shared
+//               memory in the swizzled K-major layout (128-byte swizzle for
+//               BK = 64, 64-byte swizzle for BK = 32).
+//   warp 1      allocates the accumulators in tensor memory; one lane issues
+//               tcgen05.mma (M=128, N<=256, K=16, bf16 -> fp32) for every
+//               16 columns of a stage and every 256-token half of the tile,
+//               commits each stage back to the ring and each finished tile
+//               to the epilogue.
 //   warps 2-5   epilogue: tcgen05.ld of a finished accumulator (each warp
 //               reads its own 32-lane sub-partition), bf16 conversion and
-//               coalesced stores of out[m][r]; the accumulator is released
-//               while the MMA already fills the other one.
-//   warps 6-21  decoders in two groups of eight, taking alternate stages:
+//               coalesced stores of out[m][r].  With two accumulators (BN <=
+//               256) the epilogue of one tile overlaps the next tile's MMAs.
+//   warps 6-21  decoders in groups that take turns on the ring's stages:
 //               each thread decodes a run of 32 positions of one of the
 //               tile's 128 weight rows straight into the swizzled A tile
 //               (generic-proxy stores, then fence.proxy.async).  The code
-//               words of a run are loaded two stages ahead.
-// A ring of NS stages (A 16 KB + B BN*128 bytes each) decouples producer,
-// decoders and MMA; every mbarrier wait is bounded.
+//               words of a run are loaded two turns ahead.
+// Tile shapes: BN = 512 tokens for M > 256 (a 512-column accumulator, so each
+// decoded weight feeds 512 tokens -- decoding, not the tensor core, is the
+// costly part of this GEMM), else the smallest of 32..256 that covers M.
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -45,13 +48,16 @@ __device__ int g_device_error = 0;
 
 namespace {
 
-constexpr int kBM = 128;               // weight rows per tile (MMA M)
-constexpr int kBK = 64;                // columns per stage (one 128-byte swizzle row of bf16)
-constexpr int kATile = kBM * kBK * 2;  // 16 KB
-constexpr int kProdWarp = 0, kMmaWarp = 1, kEpiWarp0 = 2, kEpiWarps = 4, kDecWarp0 = 6;
-constexpr int kGroupWarps = 8, kGroups = 2;
-constexpr int kThreads = 32 * (kDecWarp0 + kGroups * kGroupWarps);  // 704
-constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
+constexpr int kBM = 128;  // weight rows per tile (MMA M)
+constexpr int kProdWarp = 0, kMmaWarp = 1, kEpiWarp0 = 2, kEpiWarps = 4, kDecWarp0 = 6, kDecWarps = 16;
+constexpr int kThreads = 32 * (kDecWarp0 + kDecWarps);  // 704
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait: far beyond any legitimate wait
+
+// fp32 split of 1/d: kRcpHi is the nearest fp32, kRcpLo the nearest fp32 to
+// the remainder.  fma(y, kRcpHi, y * kRcpLo) is the correctly rounded y/d for
+// every y in [-510, 510] (checked exhaustively by the oracle pin tests).
+constexpr float kRcpHi = 1.0f / 147.800537109375f;
+constexpr float kRcpLo = (float)(1.0 / 147.800537109375 - (double)(1.0f / 147.800537109375f));
 
 struct PrefillParams {
   const uint32_t* codes;
@@ -62,17 +68,30 @@ struct PrefillParams {
   int nRT, nTiles;  // row tiles, total tiles
 };
 
-template <int BN>
+template <int BN, int BK>
 struct Cfg {
-  static constexpr int NS = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);  // ring stages
-  static constexpr int BTile = BN * kBK * 2;
-  static constexpr int Stage = kATile + BTile;
-  static constexpr int TmemCols = 2 * BN < 32 ? 32 : 2 * BN;  // two accumulators
-  static constexpr size_t Smem = 1024 + (size_t)NS * Stage + 256;
+  static constexpr int NACC = 2 * BN <= 512 ? 2 : 1;  // accumulators in tensor memory
+  static constexpr int NMMA = BN > 256 ? 256 : BN;    // MMA N
+  static constexpr int NH = BN / NMMA;                 // MMAs along N per 16 columns
+  static constexpr int ATile = kBM * BK * 2;
+  static constexpr int BTile = BN * BK * 2;
+  static constexpr int Stage = ATile + BTile;
+  static constexpr int NS0 = (220 * 1024) / Stage;
+  static constexpr int NS = NS0 > 8 ? 8 : NS0;         // ring stages
+  static constexpr int TmemCols = NACC * BN < 32 ? 32 : NACC * BN;
+  static constexpr int RunsPerRow = BK / 32;            // runs of 32 positions per row and stage
+  static constexpr int GroupWarps = 4 * RunsPerRow;     // decoder warps that fill one stage
+  static constexpr int Groups = kDecWarps / GroupWarps;
+  static constexpr uint32_t SBO = 8u * BK * 2u;         // bytes between 8-row groups
+  static constexpr uint32_t SwMode = BK == 64 ? 2u : 4u;  // descriptor swizzle: 128B or 64B
+  static constexpr CUtensorMapSwizzle TmaSw = BK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  static constexpr size_t Smem = 1024 + (size_t)NS * Stage + 512;
+  static_assert(BK == 64 || BK == 32, "stage width");
+  static_assert(NS >= 2, "ring too small");
 };
 
 // The words of one run (K words of positions 32q .. 32q+31 plus the spill
-// word, which wraps to word 0 for the block's last run).
+// word, which wraps to word 0 for the block's last run) and the row scale.
 template <int K>
 struct RunWords {
   uint32_t w[K + 1];
@@ -89,73 +108,68 @@ __device__ __forceinline__ void load_run(RunWords<K>& rw, const uint32_t* __rest
   rw.scale = f16_to_f32(__ldg(sc));
 }
 
-// Decode one run into the A tile: bf16(value*scale) in the 128-byte swizzled
-// K-major layout, where 16-byte chunk q of row rl sits at chunk q ^ (rl & 7).
+// Decode one run into the A tile as bf16(value*scale): 16-byte chunk c of the
+// row goes to chunk position c ^ sw, the swizzle of the row (row & 7 for the
+// 128-byte pattern, (row >> 1) & 3 for the 64-byte one).
 template <int K, int L>
-__device__ __forceinline__ void decode_run_to_tile(const RunWords<K>& rw, uint8_t* a_tile, int rl, int chunk0) {
+__device__ __forceinline__ void decode_run_to_tile(const RunWords<K>& rw, uint8_t* row, int sw, int chunk0) {
   uint32_t s[32];
   run_states<K, L>(rw.w, s);
   const float2 nmagic = make_float2(-kMagic, -kMagic);
-  const float2 rcp = make_float2(kRcpD, kRcpD), nd = make_float2(-kD, -kD);
+  const float2 rhi = make_float2(kRcpHi, kRcpHi), rlo = make_float2(kRcpLo, kRcpLo);
   const float2 sc = make_float2(rw.scale, rw.scale);
   uint32_t packed[16];
 #pragma unroll
   for (int j = 0; j < 32; j += 2) {
     const float2 y = __fadd2_rn(make_float2(__uint_as_float(code_magic(s[j])), __uint_as_float(code_magic(s[j + 1]))),
                                 nmagic);
-    // correctly rounded y/d by one residual step, then * scale, all per element
-    const float2 qv = __fmul2_rn(y, rcp);
-    const float2 e = __ffma2_rn(qv, nd, y);  // y - q*d, exact residual
-    const float2 v = __ffma2_rn(e, rcp, qv);
+    const float2 v = __ffma2_rn(y, rhi, __fmul2_rn(y, rlo));  // correctly rounded y/d
     const float2 wv = __fmul2_rn(v, sc);
     packed[j / 2] = pack_bf16x2(wv.x, wv.y);
   }
-  uint8_t* row = a_tile + rl * 128;
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const int chunk = (chunk0 + c) ^ (rl & 7);
-    *reinterpret_cast<uint4*>(row + chunk * 16) =
+  for (int c = 0; c < 4; ++c)
+    *reinterpret_cast<uint4*>(row + (((chunk0 + c) ^ sw) << 4)) =
         make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
-  }
 }
 
 __device__ __forceinline__ void report(int code) { atomicCAS(&g_device_error, 0, code); }
 
-template <int K, int L, int BN>
+template <int K, int L, int BN, int BK>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_x, const PrefillParams p) {
-  using C_ = Cfg<BN>;
-  constexpr int NS = C_::NS;
+  using C_ = Cfg<BN, BK>;
+  constexpr int NS = C_::NS, NACC = C_::NACC, NMMA = C_::NMMA, NH = C_::NH;
   constexpr int WPB = kT * K / 32;
-  constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kBM, BN);
+  constexpr int RowBytes = BK * 2;
+  constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kBM, NMMA);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  uint8_t* a_tiles = smem;                          // NS x 16 KB
-  uint8_t* b_tiles = smem + (size_t)NS * kATile;    // NS x BN*128 B
+  uint8_t* a_tiles = smem;                                // NS x ATile
+  uint8_t* b_tiles = smem + (size_t)NS * C_::ATile;       // NS x BTile
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)NS * C_::Stage);
-  uint64_t* full_a = bars;             // decoder group -> MMA (8 warp arrivals)
-  uint64_t* full_b = bars + NS;        // TMA -> MMA (1 arrival + tx bytes)
-  uint64_t* empty = bars + 2 * NS;     // MMA commit -> producer and decoders
-  uint64_t* acc_full = bars + 3 * NS;  // [2] MMA commit -> epilogue
-  uint64_t* acc_empty = bars + 3 * NS + 2;  // [2] epilogue warps -> MMA
+  uint64_t* full_a = bars;                 // decoder group -> MMA
+  uint64_t* full_b = bars + NS;            // TMA -> MMA (1 arrival + tx bytes)
+  uint64_t* empty = bars + 2 * NS;         // MMA commit -> producer and decoders
+  uint64_t* acc_full = bars + 3 * NS;      // [NACC] MMA commit -> epilogue
+  uint64_t* acc_empty = bars + 3 * NS + 2; // [NACC] epilogue warps -> MMA
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * NS + 4);
   volatile int* fail = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x;
   const int n_local = (p.nTiles - (int)blockIdx.x + G - 1) / G;
-  const int nk = (int)(p.C / kBK);
+  const int nk = (int)(p.C / BK);
   const int64_t total = (int64_t)n_local * nk;  // stages this CTA runs
-  const uint64_t deadline = kWaitNs;  // per wait
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
-      tc::mbar_init(full_a + s, kGroupWarps);
+      tc::mbar_init(full_a + s, C_::GroupWarps);
       tc::mbar_init(full_b + s, 1);
       tc::mbar_init(empty + s, 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NACC; ++b) {
       tc::mbar_init(acc_full + b, 1);
       tc::mbar_init(acc_empty + b, kEpiWarps);
     }
@@ -174,16 +188,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kProdWarp) {
     if (lane == 0) {
-      int64_t g = 0;
-      int64_t issued = 0;
+      int64_t g = 0, issued = 0;
       for (int lt = 0; lt < n_local && !*fail; ++lt) {
         const int t = (int)blockIdx.x + lt * G;
         const int m0 = (t / p.nRT) * BN;
         for (int ks = 0; ks < nk; ++ks, ++g) {
           const int s = (int)(g % NS);
-          if (g >= NS && !tc::mbar_wait(empty + s, (uint32_t)((g / NS) & 1) ^ 1u, deadline)) { *fail = 1; break; }
+          if (g >= NS && !tc::mbar_wait(empty + s, (uint32_t)((g / NS) & 1) ^ 1u, kWaitNs)) { *fail = 1; break; }
           tc::mbar_arrive_expect_tx(full_b + s, (uint32_t)C_::BTile);
-          tc::tma_load_2d(b_tiles + (size_t)s * C_::BTile, &tmap_x, full_b + s, ks * kBK, m0);
+#pragma unroll
+          for (int h = 0; h < NH; ++h)
+            tc::tma_load_2d(b_tiles + (size_t)s * C_::BTile + (size_t)h * NMMA * RowBytes, &tmap_x, full_b + s,
+                            ks * BK, m0 + h * NMMA);
           ++issued;
         }
       }
@@ -197,27 +213,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t a0 = tc::smem_u32(a_tiles), b0 = tc::smem_u32(b_tiles);
       int64_t g = 0;
       for (int lt = 0; lt < n_local && !*fail; ++lt) {
-        const int buf = lt & 1;
-        if (lt >= 2 && !tc::mbar_wait(acc_empty + buf, (uint32_t)((lt >> 1) & 1) ^ 1u, deadline)) {
-          *fail = 1;
-          break;
-        }
+        const int buf = lt % NACC, use = lt / NACC;
+        if (use >= 1 && !tc::mbar_wait(acc_empty + buf, (uint32_t)((use - 1) & 1), kWaitNs)) { *fail = 1; break; }
         tc::fence_after_sync();
         const uint32_t d = tmem + (uint32_t)(buf * BN);
+        bool ok = true;
         for (int ks = 0; ks < nk; ++ks, ++g) {
           const int s = (int)(g % NS);
           const uint32_t ph = (uint32_t)((g / NS) & 1);
-          if (!tc::mbar_wait(full_a + s, ph, deadline) || !tc::mbar_wait(full_b + s, ph, deadline)) {
-            *fail = 1;
-            break;
-          }
+          if (!tc::mbar_wait(full_a + s, ph, kWaitNs) || !tc::mbar_wait(full_b + s, ph, kWaitNs)) { ok = false; break; }
           tc::fence_after_sync();
-          const uint64_t ad = tc::desc_sw128(a0 + s * kATile), bd = tc::desc_sw128(b0 + s * C_::BTile);
+          const uint64_t ad = tc::desc_kmajor(a0 + s * C_::ATile, C_::SBO, C_::SwMode);
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)  // +32 bytes along K per MMA: +2 in the address field
-            tc::mma_bf16(d, ad + 2 * kk, bd + 2 * kk, kIdesc, (ks | kk) != 0 ? 1u : 0u);
+          for (int h = 0; h < NH; ++h) {
+            const uint64_t bd = tc::desc_kmajor(b0 + s * C_::BTile + h * NMMA * RowBytes, C_::SBO, C_::SwMode);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)  // +32 bytes along K per MMA: +2 in the address field
+              tc::mma_bf16(d + h * NMMA, ad + 2 * kk, bd + 2 * kk, kIdesc, (ks | kk) != 0 ? 1u : 0u);
+          }
           tc::mma_commit(empty + s);
         }
+        if (!ok) { *fail = 1; break; }  // no commit without MMAs behind it
         tc::mma_commit(acc_full + buf);
       }
     }
@@ -225,8 +241,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- epilogue ----------------
     const int sp = warp & 3;  // TMEM sub-partition this warp may read
     for (int lt = 0; lt < n_local; ++lt) {
-      const int buf = lt & 1;
-      const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(acc_full + buf, (uint32_t)((lt >> 1) & 1), deadline));
+      const int buf = lt % NACC, use = lt / NACC;
+      const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(acc_full + buf, (uint32_t)(use & 1), kWaitNs));
       tc::fence_after_sync();
       if (!ok) { *fail = 1; break; }
       const int t = (int)blockIdx.x + lt * G;
@@ -255,24 +271,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------- decoders ----------------
+    constexpr int GW = C_::GroupWarps, NG = C_::Groups;
     const int dw = warp - kDecWarp0;       // 0..15
-    const int grp = dw / kGroupWarps;      // stages g with g % 2 == grp
-    const int gw = dw % kGroupWarps;
+    const int grp = dw / GW;               // this group fills stages g with g % NG == grp
+    const int gw = dw % GW;
     const int rl = (gw & 3) * 32 + lane;   // tile row of this thread
-    const int h = gw >> 2;                 // which 32-column half of a stage
+    const int h = gw >> 2;                 // which run of the stage
+    const int sw = BK == 64 ? (rl & 7) : ((rl >> 1) & 3);
     auto fetch = [&](RunWords<K>& rw, int64_t g) {
       if (g >= total) return;
       const int lt = (int)(g / nk), ks = (int)(g % nk);
       const int t = (int)blockIdx.x + lt * G;
       int64_t r = (int64_t)(t % p.nRT) * kBM + rl;
       if (r >= p.R) r = p.R - 1;  // rows past the end decode row R-1 and are never stored
-      const uint32_t* blk = p.codes + (r * p.nb + (ks >> 2)) * WPB;
-      load_run<K>(rw, blk, 2 * (ks & 3) + h, p.scales + r);
+      const int c = ks * BK + 32 * h;  // first column of the run
+      load_run<K>(rw, p.codes + (r * p.nb + c / kT) * WPB, (c % kT) / 32, p.scales + r);
     };
     auto process = [&](const RunWords<K>& rw, int64_t g) -> bool {
       const int s = (int)(g % NS);
-      if (g >= NS && !tc::mbar_wait(empty + s, (uint32_t)((g / NS) & 1) ^ 1u, deadline)) return false;
-      decode_run_to_tile<K, L>(rw, a_tiles + (size_t)s * kATile, rl, 4 * h);
+      if (g >= NS && !tc::mbar_wait(empty + s, (uint32_t)((g / NS) & 1) ^ 1u, kWaitNs)) return false;
+      decode_run_to_tile<K, L>(rw, a_tiles + (size_t)s * C_::ATile + rl * RowBytes, sw, 4 * h);
       tc::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(full_a + s);
@@ -281,15 +299,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     RunWords<K> ra, rb;
     int64_t g = grp;
     fetch(ra, g);
-    fetch(rb, g + 2);
+    fetch(rb, g + NG);
     while (g < total) {
       if (!process(ra, g)) { *fail = 1; break; }
-      fetch(ra, g + 4);
-      g += 2;
+      fetch(ra, g + 2 * NG);
+      g += NG;
       if (g >= total) break;
       if (!process(rb, g)) { *fail = 1; break; }
-      fetch(rb, g + 4);
-      g += 2;
+      fetch(rb, g + 2 * NG);
+      g += NG;
     }
   }
 
@@ -322,24 +340,24 @@ int sm_count() {
   return n;
 }
 
-template <int K, int L, int BN>
+template <int K, int L, int BN, int BK>
 cudaError_t prefill_launch(PrefillParams p, const uint16_t* x, cudaStream_t st) {
+  using C_ = Cfg<BN, BK>;
   auto fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
   CUtensorMap map;
   const cuuint64_t dims[2] = {(cuuint64_t)p.C, (cuuint64_t)p.M};
   const cuuint64_t strides[1] = {(cuuint64_t)p.C * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)BN};
+  const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)C_::NMMA};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult cr = fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box,
-                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, C_::TmaSw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  auto kern = prefill_kernel<K, L, BN>;
+  auto kern = prefill_kernel<K, L, BN, BK>;
   static bool attr_set = false;  // per instantiation
   if (!attr_set) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<BN>::Smem);
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_::Smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -347,16 +365,17 @@ cudaError_t prefill_launch(PrefillParams p, const uint16_t* x, cudaStream_t st) 
   p.nTiles = p.nRT * ((p.M + BN - 1) / BN);
   const int sms = sm_count();
   const int grid = p.nTiles < sms ? p.nTiles : sms;
-  kern<<<grid, kThreads, Cfg<BN>::Smem, st>>>(map, p);
+  kern<<<grid, kThreads, C_::Smem, st>>>(map, p);
   return cudaGetLastError();
 }
 
 template <int K, int L>
 cudaError_t prefill_bn(const PrefillParams& p, const uint16_t* x, cudaStream_t st) {
-  if (p.M <= 32) return prefill_launch<K, L, 32>(p, x, st);
-  if (p.M <= 64) return prefill_launch<K, L, 64>(p, x, st);
-  if (p.M <= 128) return prefill_launch<K, L, 128>(p, x, st);
-  return prefill_launch<K, L, 256>(p, x, st);
+  if (p.M <= 32) return prefill_launch<K, L, 32, 64>(p, x, st);
+  if (p.M <= 64) return prefill_launch<K, L, 64, 64>(p, x, st);
+  if (p.M <= 128) return prefill_launch<K, L, 128, 64>(p, x, st);
+  if (p.M <= 256) return prefill_launch<K, L, 256, 64>(p, x, st);
+  return prefill_launch<K, L, 512, 32>(p, x, st);
 }
 
 }  // namespace

@@ -133,17 +133,18 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// Shared-memory matrix descriptor of a K-major operand in the 128-byte
-// swizzled canonical layout: rows of 128 bytes, 8-row groups 1024 bytes apart
-// (stride byte offset), leading byte offset unused for this layout,
-// descriptor version 1, swizzle mode 2 (128B).
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+// Shared-memory matrix descriptor of a K-major operand in a swizzled
+// canonical layout: start address, leading byte offset (unused by the
+// swizzled K-major layouts), stride byte offset = bytes between consecutive
+// 8-row groups, descriptor version 1 (bit 46), swizzle mode in bits 61-63
+// (2 = 128-byte, 4 = 64-byte).
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t saddr, uint32_t sbo, uint32_t swizzle_mode) {
   uint64_t d = 0;
   d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
   d |= (uint64_t)1 << 16;
-  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
   d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
+  d |= (uint64_t)(swizzle_mode & 7u) << 61;
   return d;
 }
 
