@@ -57,24 +57,49 @@ __device__ __forceinline__ uint16_t swiglu_chain(float gate, float up) {
   return f32_to_bf16_rn(__fmul_rn(silu, u));
 }
 
+// A half block: runs 7..4 (block words [0, 4K)) or runs 3..0 (words
+// [4K, 8K)), plus the spill word of its last run (word 4K, or word 0 where
+// the block wraps).
+template <int K, int NMAT>
+struct HalfBlock {
+  uint32_t w[NMAT][4 * K + 1];
+};
+
+template <int K, int NMAT>
+__device__ __forceinline__ void load_half(HalfBlock<K, NMAT>& hbk, const uint32_t* const (&crow)[NMAT], int ci) {
+  constexpr int WPB = kT * K / 32;
+  const int b = ci >> 1, hb = ci & 1;
+#pragma unroll
+  for (int t = 0; t < NMAT; ++t) {
+    const uint32_t* blk = crow[t] + (int64_t)b * WPB;
+    const uint4* v4 = reinterpret_cast<const uint4*>(blk + hb * 4 * K);
+#pragma unroll
+    for (int i = 0; i < K; ++i) {
+      const uint4 v = __ldg(v4 + i);
+      hbk.w[t][4 * i] = v.x; hbk.w[t][4 * i + 1] = v.y; hbk.w[t][4 * i + 2] = v.z; hbk.w[t][4 * i + 3] = v.w;
+    }
+    hbk.w[t][4 * K] = __ldg(blk + (hb ? 0 : 4 * K));
+  }
+}
+
 template <int K, int L, int M, bool GU>
-__global__ void __launch_bounds__(256) mv1_kernel(const Mv1Params p) {
+__global__ void __launch_bounds__(512) mv1_kernel(const Mv1Params p) {
   extern __shared__ __align__(16) float smem[];
   constexpr int NMAT = GU ? 2 : 1;
   constexpr int WPB = kT * K / 32;
+  constexpr int HB = kT / 2;  // positions per half block
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, S = blockDim.x >> 5;
-  float* xs = smem + warp * (M * kT);
-  float* red = smem + S * M * kT;
+  float* xs = smem + warp * (M * HB);
+  float* red = smem + S * M * HB;
 
   const int64_t row = (int64_t)blockIdx.x * 32 + lane;
   const int64_t rr = row < p.R ? row : p.R - 1;  // clamped rows load valid memory and store nothing
-  const int b0 = (int)((int64_t)warp * p.nb / S);
-  const int b1 = (int)((int64_t)(warp + 1) * p.nb / S);
+  const int c0 = (int)((int64_t)warp * 2 * p.nb / S);  // this warp's half blocks [c0, c1)
+  const int c1 = (int)((int64_t)(warp + 1) * 2 * p.nb / S);
 
-  const uint4* crow[NMAT];
+  const uint32_t* crow[NMAT];
 #pragma unroll
-  for (int t = 0; t < NMAT; ++t)
-    crow[t] = reinterpret_cast<const uint4*>(p.codes[t] + rr * (int64_t)p.nb * WPB);
+  for (int t = 0; t < NMAT; ++t) crow[t] = p.codes[t] + rr * (int64_t)p.nb * WPB;
 
   float2 acc[NMAT][M][2];
 #pragma unroll
@@ -83,36 +108,27 @@ __global__ void __launch_bounds__(256) mv1_kernel(const Mv1Params p) {
     for (int m = 0; m < M; ++m) acc[t][m][0] = acc[t][m][1] = make_float2(0.f, 0.f);
   const float2 nmagic = make_float2(-kMagic, -kMagic);
 
-  for (int b = b0; b < b1; ++b) {
-    // codes of block b of this lane's row (issued first; x staging overlaps their latency)
-    uint32_t cw[NMAT][WPB];
-#pragma unroll
-    for (int t = 0; t < NMAT; ++t)
-#pragma unroll
-      for (int i = 0; i < WPB / 4; ++i) {
-        const uint4 v = __ldg(crow[t] + (int64_t)b * (WPB / 4) + i);
-        cw[t][4 * i] = v.x; cw[t][4 * i + 1] = v.y; cw[t][4 * i + 2] = v.z; cw[t][4 * i + 3] = v.w;
-      }
-    // x[:, block b] as fp32 in this warp's shared tile
+  auto process = [&](const HalfBlock<K, NMAT>& hbk, int ci) {
+    const int b = ci >> 1, hb = ci & 1;
+    // x of this half block (positions 128*(1-hb) .. +127 of block b) as fp32
+    const int pos0 = 128 * (1 - hb);
     __syncwarp();
 #pragma unroll
     for (int m = 0; m < M; ++m) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(p.x + (int64_t)m * p.C + (int64_t)b * kT) + lane);
-      float4* dst = reinterpret_cast<float4*>(xs + m * kT + 8 * lane);
-      dst[0] = make_float4(bf16lo_to_f32(v.x), bf16hi_to_f32(v.x), bf16lo_to_f32(v.y), bf16hi_to_f32(v.y));
-      dst[1] = make_float4(bf16lo_to_f32(v.z), bf16hi_to_f32(v.z), bf16lo_to_f32(v.w), bf16hi_to_f32(v.w));
+      const uint2 v = __ldg(reinterpret_cast<const uint2*>(p.x + (int64_t)m * p.C + (int64_t)b * kT + pos0) + lane);
+      *reinterpret_cast<float4*>(xs + m * HB + 4 * lane) =
+          make_float4(bf16lo_to_f32(v.x), bf16hi_to_f32(v.x), bf16lo_to_f32(v.y), bf16hi_to_f32(v.y));
     }
     __syncwarp();
-    // eight runs of 32 positions; run q holds positions 32q .. 32q+31 in
-    // words (7-q)*K .. (7-q)*K+K-1, the spill word follows (wrapping for q = 0)
+    // runs r4 = 0..3 of the half: q = 7 - 4*hb - r4 holds positions 32q .. 32q+31
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
+    for (int r4 = 0; r4 < 4; ++r4) {
+      const int xq = 32 * (3 - r4);  // offset of run q inside the half block's positions
 #pragma unroll
       for (int t = 0; t < NMAT; ++t) {
         uint32_t w[K + 1];
 #pragma unroll
-        for (int i = 0; i < K; ++i) w[i] = cw[t][(7 - q) * K + i];
-        w[K] = cw[t][((8 - q) * K) % WPB];
+        for (int i = 0; i <= K; ++i) w[i] = hbk.w[t][r4 * K + i];
         uint32_t s[32];
         run_states<K, L>(w, s);
 #pragma unroll
@@ -123,13 +139,22 @@ __global__ void __launch_bounds__(256) mv1_kernel(const Mv1Params p) {
                                                    __uint_as_float(code_magic(s[4 * j4 + 3]))), nmagic);
 #pragma unroll
           for (int m = 0; m < M; ++m) {
-            const float4 xv = *reinterpret_cast<const float4*>(xs + m * kT + 32 * q + 4 * j4);
+            const float4 xv = *reinterpret_cast<const float4*>(xs + m * HB + xq + 4 * j4);
             acc[t][m][0] = __ffma2_rn(ya, make_float2(xv.x, xv.y), acc[t][m][0]);
             acc[t][m][1] = __ffma2_rn(yb, make_float2(xv.z, xv.w), acc[t][m][1]);
           }
         }
       }
     }
+  };
+
+  // Half blocks in order; each lane's loads are issued at the top of the
+  // half block and the warp's x staging overlaps their latency.  (Loading the
+  // next half block ahead into a second register set measured slower.)
+  for (int ci = c0; ci < c1; ++ci) {
+    HalfBlock<K, NMAT> hbk;
+    load_half<K, NMAT>(hbk, crow, ci);
+    process(hbk, ci);
   }
 
   // fold the S warps' partial sums of each row in a fixed order
@@ -160,22 +185,41 @@ __global__ void __launch_bounds__(256) mv1_kernel(const Mv1Params p) {
   }
 }
 
-// Warps per CTA: the row's blocks are split S ways.
-static int mv1_splits(int nb) { return nb < 4 ? nb : 4; }
+// Warps per CTA (the row's half blocks are split S ways): as many as keep
+// four CTAs resident per SM with this instantiation's register count, so the
+// R/32 CTAs of a large matrix run in a single wave; never more than the row
+// has half blocks, and at most 16.
+static int mv1_splits(int nb, int regs) {
+  int s = 65536 / (4 * 32 * (regs > 0 ? regs : 64));
+  if (s > 2 * nb) s = 2 * nb;
+  if (s > 16) s = 16;
+  return s < 1 ? 1 : s;
+}
+
+template <int K, int L, int M, bool GU>
+static cudaError_t mv1_launch(const Mv1Params& p, cudaStream_t st) {
+  static int regs = 0;  // per instantiation
+  if (!regs) {
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, mv1_kernel<K, L, M, GU>) != cudaSuccess) return cudaGetLastError();
+    regs = a.numRegs;
+  }
+  const int S = mv1_splits(p.nb, regs);
+  const int nmat = GU ? 2 : 1;
+  const size_t sm = (size_t)S * M * (kT / 2) * sizeof(float) + (size_t)nmat * S * M * 32 * sizeof(float);
+  const dim3 grid((unsigned)((p.R + 31) / 32)), block(32 * S);
+  mv1_kernel<K, L, M, GU><<<grid, block, sm, st>>>(p);
+  return cudaGetLastError();
+}
 
 template <int K, int L, bool GU>
 static cudaError_t mv1_launch_m(const Mv1Params& p, int M, cudaStream_t st) {
-  const int S = mv1_splits(p.nb);
-  const int nmat = GU ? 2 : 1;
-  const size_t sm = (size_t)S * M * kT * sizeof(float) + (size_t)nmat * S * M * 32 * sizeof(float);
-  const dim3 grid((unsigned)((p.R + 31) / 32)), block(32 * S);
   switch (M) {
-    case 1: mv1_kernel<K, L, 1, GU><<<grid, block, sm, st>>>(p); break;
-    case 2: mv1_kernel<K, L, 2, GU><<<grid, block, sm, st>>>(p); break;
-    case 3: mv1_kernel<K, L, 3, GU><<<grid, block, sm, st>>>(p); break;
-    default: mv1_kernel<K, L, 4, GU><<<grid, block, sm, st>>>(p); break;
+    case 1: return mv1_launch<K, L, 1, GU>(p, st);
+    case 2: return mv1_launch<K, L, 2, GU>(p, st);
+    case 3: return mv1_launch<K, L, 3, GU>(p, st);
+    default: return mv1_launch<K, L, 4, GU>(p, st);
   }
-  return cudaGetLastError();
 }
 
 template <bool GU>
