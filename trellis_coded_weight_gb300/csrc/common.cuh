@@ -46,6 +46,19 @@ __device__ __forceinline__ float value_rn(float y) {
   return __fmaf_rn(e, kRcpD, q);
 }
 
+// fp32 split of 1/d: kRcpHi = kRcpD is the nearest fp32, kRcpLo the nearest
+// fp32 to the remainder (1/d in double minus kRcpHi).  fma(y, kRcpHi,
+// y * kRcpLo) is the correctly rounded y/d for every y in [-510, 510]: one
+// rounding of a 48-bit-accurate product (checked exhaustively against exact
+// rational arithmetic by the oracle pin tests).
+constexpr float kRcpHi = kRcpD;
+constexpr float kRcpLo = (float)(1.0 / 147.800537109375 - (double)(1.0f / 147.800537109375f));
+
+// Correctly rounded (y0/d, y1/d) for exact integer-valued y, packed f32x2.
+__device__ __forceinline__ float2 value_rn2(float2 y) {
+  return __ffma2_rn(y, make_float2(kRcpHi, kRcpHi), __fmul2_rn(y, make_float2(kRcpLo, kRcpLo)));
+}
+
 // Round two floats to bf16 (nearest even) and pack them, a in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   uint32_t r;

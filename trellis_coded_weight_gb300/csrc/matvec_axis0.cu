@@ -31,6 +31,7 @@
 namespace trellis {
 
 constexpr int kAx0Warps = 4;
+constexpr int kAx0Chunk = 8;  // rows per prefetch chunk
 constexpr int64_t kAx0TargetCtas = 152 * 5;
 
 struct Ax0Plan {
@@ -124,21 +125,38 @@ __global__ void __launch_bounds__(32 * kAx0Warps) ax0_kernel(const Ax0Params p) 
     }
   };
 
-  int rl = warp;
-  for (; rl + 3 * kAx0Warps < nr; rl += 4 * kAx0Warps) {
-    uint32_t a[4], b[4];
+  // This warp's rows are warp, warp + W, ... (W warps per CTA).  They go in
+  // chunks of kAx0Chunk rows; the code words of the next chunk load while the
+  // current chunk decodes.  Rows past the slice load a valid row and are skipped.
+  const int nw = nr > warp ? (nr - warp + kAx0Warps - 1) / kAx0Warps : 0;
+  const int nch = (nw + kAx0Chunk - 1) / kAx0Chunk;
+  auto load_chunk = [&](uint32_t (&a)[kAx0Chunk], uint32_t (&b)[kAx0Chunk], int ch) {
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const uint32_t* rw = base + (r0 + rl + u * kAx0Warps) * rowWords;
+    for (int u = 0; u < kAx0Chunk; ++u) {
+      int i = ch * kAx0Chunk + u;
+      if (i >= nw) i = nw - 1;
+      const uint32_t* rw = base + (r0 + warp + (int64_t)i * kAx0Warps) * rowWords;
       a[u] = __ldg(rw + wa);
       b[u] = __ldg(rw + wb);
     }
+  };
+  auto run_chunk = [&](const uint32_t (&a)[kAx0Chunk], const uint32_t (&b)[kAx0Chunk], int ch) {
 #pragma unroll
-    for (int u = 0; u < 4; ++u) body(a[u], b[u], rl + u * kAx0Warps);
-  }
-  for (; rl < nr; rl += kAx0Warps) {
-    const uint32_t* rw = base + (r0 + rl) * rowWords;
-    body(__ldg(rw + wa), __ldg(rw + wb), rl);
+    for (int u = 0; u < kAx0Chunk; ++u) {
+      const int i = ch * kAx0Chunk + u;
+      if (i < nw) body(a[u], b[u], warp + i * kAx0Warps);
+    }
+  };
+  if (nch > 0) {
+    uint32_t a0[kAx0Chunk], b0[kAx0Chunk], a1[kAx0Chunk], b1[kAx0Chunk];
+    load_chunk(a0, b0, 0);
+    for (int ch = 0; ch < nch; ch += 2) {
+      if (ch + 1 < nch) load_chunk(a1, b1, ch + 1);
+      run_chunk(a0, b0, ch);
+      if (ch + 1 >= nch) break;
+      if (ch + 2 < nch) load_chunk(a0, b0, ch + 2);
+      run_chunk(a1, b1, ch + 1);
+    }
   }
 
   // fold the warps of this CTA

@@ -53,11 +53,6 @@ constexpr int kProdWarp = 0, kMmaWarp = 1, kEpiWarp0 = 2, kEpiWarps = 4, kDecWar
 constexpr int kThreads = 32 * (kDecWarp0 + kDecWarps);  // 704
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait: far beyond any legitimate wait
 
-// fp32 split of 1/d: kRcpHi is the nearest fp32, kRcpLo the nearest fp32 to
-// the remainder.  fma(y, kRcpHi, y * kRcpLo) is the correctly rounded y/d for
-// every y in [-510, 510] (checked exhaustively by the oracle pin tests).
-constexpr float kRcpHi = 1.0f / 147.800537109375f;
-constexpr float kRcpLo = (float)(1.0 / 147.800537109375 - (double)(1.0f / 147.800537109375f));
 
 struct PrefillParams {
   const uint32_t* codes;
@@ -116,14 +111,13 @@ __device__ __forceinline__ void decode_run_to_tile(const RunWords<K>& rw, uint8_
   uint32_t s[32];
   run_states<K, L>(rw.w, s);
   const float2 nmagic = make_float2(-kMagic, -kMagic);
-  const float2 rhi = make_float2(kRcpHi, kRcpHi), rlo = make_float2(kRcpLo, kRcpLo);
   const float2 sc = make_float2(rw.scale, rw.scale);
   uint32_t packed[16];
 #pragma unroll
   for (int j = 0; j < 32; j += 2) {
     const float2 y = __fadd2_rn(make_float2(__uint_as_float(code_magic(s[j])), __uint_as_float(code_magic(s[j + 1]))),
                                 nmagic);
-    const float2 v = __ffma2_rn(y, rhi, __fmul2_rn(y, rlo));  // correctly rounded y/d
+    const float2 v = value_rn2(y);  // correctly rounded y/d
     const float2 wv = __fmul2_rn(v, sc);
     packed[j / 2] = pack_bf16x2(wv.x, wv.y);
   }
