@@ -73,7 +73,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.th = threading.Thread(target=self._read, daemon=True)
             self.th.start()
@@ -396,6 +396,43 @@ def run_reference(args):
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_single(kind: str, k: str, M: str):
+    """Four launches of one kernel on the full-size workload (for ncu: -s 3 -c 1)."""
+    import torch
+    from trellis_coded_weight_gb300 import binding as tb
+    from trellis_coded_weight_gb300 import build as tbuild
+    from trellis_coded_weight_gb300 import inputs
+    k, M = int(k), int(M)
+    dev = torch.device("cuda", 0)
+    tbuild.build()
+    tb.load()
+    codes = _dev_words(inputs.random_words(inputs.SEED_CODES, (R, C * k // 32)), dev)
+    codes2 = _dev_words(inputs.random_words(inputs.SEED_UP, (R, C * k // 32)), dev)
+    sc = _dev_f16(inputs.uniform_f16(inputs.SEED_SCALES, (R,)), dev)
+    g1, g0 = tb.Geometry(k, L, T, 1, R, C), tb.Geometry(k, L, T, 0, R, C)
+    if kind == "axis1":
+        x = _dev_bf16(inputs.normal_bf16(inputs.SEED_X, (M, C)), dev)
+        fn = lambda: tb.matvec_axis1(codes, sc, x, g1)
+    elif kind == "gateup":
+        x = _dev_bf16(inputs.normal_bf16(inputs.SEED_X, (M, C)), dev)
+        fn = lambda: tb.gateup_swiglu(codes, sc, codes2, sc, x, g1)
+    elif kind == "axis0":
+        x = _dev_bf16(inputs.normal_bf16(inputs.SEED_X, (M, R), 0.5), dev)
+        ws = tb.new_workspace(M, g0, dev)
+        fn = lambda: tb.matvec_axis0(codes, sc, x, g0, ws)
+    elif kind == "expand":
+        fn = lambda: tb.expand_bf16(codes, sc, g1)
+    elif kind == "prefill":
+        x = _dev_bf16(inputs.normal_bf16(inputs.SEED_X, (M, C)), dev)
+        fn = lambda: tb.gemm_prefill(codes, sc, x, g1)
+    else:
+        raise SystemExit(f"unknown kind {kind}")
+    for _ in range(4):
+        fn()
+    torch.cuda.synchronize(dev)
+    print(json.dumps({"single": kind, "k": k, "M": M, "device_error": tb.device_error()}))
+
+
 def kernel_source_hash(name: str) -> str:
     import hashlib
     h = hashlib.sha256()
@@ -421,12 +458,18 @@ def measured_traffic(kernel_file: str):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--extra", action="store_true", help="also time gate/up, axis-0 and expand (stderr)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--single", nargs=3, metavar=("KIND", "K", "M"),
+                    help="profiling aid: run 4 launches of one kernel at full size and exit "
+                         "(KIND: axis1, gateup, axis0, expand, prefill)")
     args = ap.parse_args()
+    if args.single:
+        run_single(*args.single)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
 
