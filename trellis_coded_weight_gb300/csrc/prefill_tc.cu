@@ -32,6 +32,7 @@
 // decoded weight feeds 512 tokens -- decoding, not the tensor core, is the
 // costly part of this GEMM), else the smallest of 32..256 that covers M.
 #include <cstdint>
+#include <cstring>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -61,6 +62,7 @@ struct PrefillParams {
   int64_t R, C;
   int M, nb;
   int nRT, nTiles;  // row tiles, total tiles
+  int tma_out;      // 1: out written by TMA tensor stores (R % 8 == 0)
 };
 
 template <int BN, int BK>
@@ -71,7 +73,8 @@ struct Cfg {
   static constexpr int ATile = kBM * BK * 2;
   static constexpr int BTile = BN * BK * 2;
   static constexpr int Stage = ATile + BTile;
-  static constexpr int NS0 = (220 * 1024) / Stage;
+  static constexpr int EpiBytes = kEpiWarps * 2 * 32 * 32 * 2;  // per warp: two 32x32 bf16 sub-tiles
+  static constexpr int NS0 = (220 * 1024 - EpiBytes) / Stage;
   static constexpr int NS = NS0 > 8 ? 8 : NS0;         // ring stages
   static constexpr int TmemCols = NACC * BN < 32 ? 32 : NACC * BN;
   static constexpr int RunsPerRow = BK / 32;            // runs of 32 positions per row and stage
@@ -80,7 +83,7 @@ struct Cfg {
   static constexpr uint32_t SBO = 8u * BK * 2u;         // bytes between 8-row groups
   static constexpr uint32_t SwMode = BK == 64 ? 2u : 4u;  // descriptor swizzle: 128B or 64B
   static constexpr CUtensorMapSwizzle TmaSw = BK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-  static constexpr size_t Smem = 1024 + (size_t)NS * Stage + 512;
+  static constexpr size_t Smem = 1024 + (size_t)NS * Stage + EpiBytes + 512;
   static_assert(BK == 64 || BK == 32, "stage width");
   static_assert(NS >= 2, "ring too small");
 };
@@ -131,7 +134,8 @@ __device__ __forceinline__ void report(int code) { atomicCAS(&g_device_error, 0,
 
 template <int K, int L, int BN, int BK>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap tmap_x, const PrefillParams p) {
+    prefill_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_out,
+                   const PrefillParams p) {
   using C_ = Cfg<BN, BK>;
   constexpr int NS = C_::NS, NACC = C_::NACC, NMMA = C_::NMMA, NH = C_::NH;
   constexpr int WPB = kT * K / 32;
@@ -142,7 +146,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* a_tiles = smem;                                // NS x ATile
   uint8_t* b_tiles = smem + (size_t)NS * C_::ATile;       // NS x BTile
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)NS * C_::Stage);
+  uint8_t* epi_stage = smem + (size_t)NS * C_::Stage;     // kEpiWarps x 2 x [32 tokens][32 rows] bf16
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_stage + C_::EpiBytes);
   uint64_t* full_a = bars;                 // decoder group -> MMA
   uint64_t* full_b = bars + NS;            // TMA -> MMA (1 arrival + tx bytes)
   uint64_t* empty = bars + 2 * NS;         // MMA commit -> producer and decoders
@@ -234,20 +239,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < kEpiWarp0 + kEpiWarps) {
     // ---------------- epilogue ----------------
     const int sp = warp & 3;  // TMEM sub-partition this warp may read
+    int ec = 0;               // staging buffers alternate per stored chunk
     for (int lt = 0; lt < n_local; ++lt) {
       const int buf = lt % NACC, use = lt / NACC;
       const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(acc_full + buf, (uint32_t)(use & 1), kWaitNs));
       tc::fence_after_sync();
       if (!ok) { *fail = 1; break; }
       const int t = (int)blockIdx.x + lt * G;
-      const int64_t row = (int64_t)(t % p.nRT) * kBM + 32 * sp + lane;
+      const int64_t rbase = (int64_t)(t % p.nRT) * kBM + 32 * sp;  // first row of this warp's 32
+      const int64_t row = rbase + lane;
       const int m0 = (t / p.nRT) * BN;
+      uint16_t* my_stage = reinterpret_cast<uint16_t*>(epi_stage) + (size_t)(warp - kEpiWarp0) * 2 * 32 * 32;
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 32) {
         uint32_t v[32];
         tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * sp) << 16) + (uint32_t)(buf * BN + c0), v);
         tc::tmem_ld_wait();
-        if (row < p.R) {
+        if (p.tma_out) {
+          // stage [32 tokens][32 rows] bf16, then one lane stores the box with TMA
+          uint16_t* st = my_stage + (ec++ & 1) * 32 * 32;
+          if (lane == 0) tc::bulk_wait_read<1>();  // the previous use of this buffer has been read
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            uint16_t o;
+            asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(o) : "f"(__uint_as_float(v[i])));
+            st[i * 32 + lane] = o;
+          }
+          tc::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && m0 + c0 < p.M && rbase < p.R) {
+            tc::tma_store_2d(&tmap_out, st, (int)rbase, m0 + c0);
+            tc::bulk_commit();
+          }
+        } else if (row < p.R) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int m = m0 + c0 + i;
@@ -263,6 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(acc_empty + buf);
     }
+    if (lane == 0) tc::bulk_wait<0>();  // all tensor stores of this warp complete before exit
+    __syncwarp();
   } else {
     // ---------------- decoders ----------------
     constexpr int GW = C_::GroupWarps, NG = C_::Groups;
@@ -339,15 +366,29 @@ cudaError_t prefill_launch(PrefillParams p, const uint16_t* x, cudaStream_t st) 
   using C_ = Cfg<BN, BK>;
   auto fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
-  CUtensorMap map;
-  const cuuint64_t dims[2] = {(cuuint64_t)p.C, (cuuint64_t)p.M};
-  const cuuint64_t strides[1] = {(cuuint64_t)p.C * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)C_::NMMA};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult cr = fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box,
-                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, C_::TmaSw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  CUtensorMap map, omap;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)p.C, (cuuint64_t)p.M};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.C * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)C_::NMMA};
+    const cuuint32_t estr[2] = {1, 1};
+    if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, C_::TmaSw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  memset(&omap, 0, sizeof(omap));
+  p.tma_out = 0;
+  if (p.R % 8 == 0) {  // out rows are 16-byte multiples: tensor stores of [32 tokens][32 rows] boxes
+    const cuuint64_t dims[2] = {(cuuint64_t)p.R, (cuuint64_t)p.M};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.R * 2};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    if (fn(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.out, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+        CUDA_SUCCESS)
+      p.tma_out = 1;
+  }
   auto kern = prefill_kernel<K, L, BN, BK>;
   static bool attr_set = false;  // per instantiation
   if (!attr_set) {
@@ -359,7 +400,7 @@ cudaError_t prefill_launch(PrefillParams p, const uint16_t* x, cudaStream_t st) 
   p.nTiles = p.nRT * ((p.M + BN - 1) / BN);
   const int sms = sm_count();
   const int grid = p.nTiles < sms ? p.nTiles : sms;
-  kern<<<grid, kThreads, C_::Smem, st>>>(map, p);
+  kern<<<grid, kThreads, C_::Smem, st>>>(map, omap, p);
   return cudaGetLastError();
 }
 
