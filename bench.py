@@ -305,6 +305,22 @@ def run_extra(args, dev, stream, tb, inputs, l2):
         torch.cuda.synchronize(dev)
         return a.elapsed_time(b) / n
 
+    # the decode MLP block (gate/up SwiGLU + down), replayed as CUDA graphs
+    for ku, kd in ((2, 2), (3, 3)):
+        g_up, g_dn = tb.Geometry(ku, L, T, 1, R, C), tb.Geometry(kd, L, T, 0, R, C)
+        sc = _dev_f16(inputs.uniform_f16(inputs.SEED_SCALES, (R,)), dev)
+        wsets = [[_dev_words(inputs.random_words(7000 + 10 * i + j, (R, C * (ku if j < 2 else kd) // 32)), dev)
+                  for j in range(3)] for i in range(3)]
+        for M in MS:
+            graphs = [tb.MlpDecodeGraph(w[0], sc, w[1], sc, w[2], sc, g_up, g_dn, M) for w in wsets]
+            for gr in graphs:
+                gr.x.copy_(_dev_bf16(inputs.normal_bf16(inputs.SEED_X, (M, C)), dev))
+            ms = timed(lambda i: graphs[i].replay(), len(graphs))
+            per = packed_bytes(ku) * 2 + packed_bytes(kd)
+            res.append({"kind": "mlp_graph", "k_up": ku, "k_down": kd, "M": M, "us": ms * 1e3,
+                        "packed_GBps": per / (ms * 1e-3) / 1e9})
+            del graphs
+        del wsets
     for kind, ks in (("gateup", (2, 3)), ("axis0", (2, 3)), ("expand", (2, 3, 4))):
         for k in ks:
             per = packed_bytes(k) * (2 if kind == "gateup" else 1)

@@ -176,6 +176,26 @@ int trellis_gateup_swiglu(const uint32_t *gcodes, const uint16_t *gscales, const
                           const trellis_geom_t *g, trellis_stream_t stream);
 
 /*
+ * trellis_mlp_decode -- the decode-time MLP block of the pages' Qwen3MLP
+ * ("qwen3_5.ts" diff page, Qwen3MLP.forward for M <= 4: the fused gate/up
+ * SwiGLU kernel followed by the down projection):
+ *   hidden = trellis_gateup_swiglu(gate, up, x)        [M][I] bf16
+ *   out    = trellis_matvec_axis0(down, hidden)        [M][H] bf16
+ * Two kernel launches on `stream`, no allocation and no synchronisation, so
+ * the call can be captured into a CUDA graph.
+ *   g_up    axis-1 geometry of gate and up: rows = I (intermediate), cols = H
+ *   g_down  axis-0 geometry of down (stored W^T): rows = I, cols = H
+ *   x [M][H]   hidden [M][I] (caller-owned, written)   out [M][H]
+ *   workspace: as for trellis_matvec_axis0 with (M, g_down).
+ * Requires 1 <= M <= 4; k may differ between the two geometries.
+ */
+int trellis_mlp_decode(const uint32_t *gcodes, const uint16_t *gscales, const uint32_t *ucodes,
+                       const uint16_t *uscales, const uint32_t *dcodes, const uint16_t *dscales,
+                       const uint16_t *x, uint16_t *hidden, uint16_t *out, int M,
+                       const trellis_geom_t *g_up, const trellis_geom_t *g_down, void *workspace,
+                       size_t workspace_bytes, trellis_stream_t stream);
+
+/*
  * trellis_gemm_prefill -- prefill GEMM over an axis-1 matrix for any M >= 1
  * (intended for M > 4) ("trellis-tiled-prefill.ts": tiledTrellisPrefill and
  * the expand + matmul path of TrellisLinear.forward).  Weight tiles are

@@ -99,3 +99,13 @@ def test_workspace_grows_with_M(lib):
     g0 = G(axis=0, rows=17408, cols=5120)
     sizes = [lib.trellis_workspace_bytes(m, ctypes.byref(g0)) for m in (1, 2, 3, 4)]
     assert sizes == sorted(sizes) and sizes[0] > 0
+
+
+def test_mlp_decode_errors_before_launch(lib):
+    gu, gd = G(axis=1), G(axis=0)
+    need = lib.trellis_workspace_bytes(2, ctypes.byref(gd))
+    args = [A] * 9
+    assert lib.trellis_mlp_decode(*args, 2, ctypes.byref(gu), ctypes.byref(G(axis=0, rows=32)), A, need, None) == -1
+    assert lib.trellis_mlp_decode(*args, 2, ctypes.byref(gd), ctypes.byref(gd), A, need, None) == -4
+    assert lib.trellis_mlp_decode(*args, 5, ctypes.byref(gu), ctypes.byref(gd), A, need, None) == -2
+    assert lib.trellis_mlp_decode(*args, 2, ctypes.byref(gu), ctypes.byref(gd), A, need - 16, None) == -5

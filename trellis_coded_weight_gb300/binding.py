@@ -27,7 +27,7 @@ STATUS_NAMES = {0: "TRELLIS_OK", -1: "TRELLIS_EGEOM", -2: "TRELLIS_EM", -3: "TRE
 
 EXPORTS = ("trellis_abi_version", "trellis_status_string", "trellis_check_geom", "trellis_expand_bf16",
            "trellis_matvec_axis1", "trellis_matvec_axis0", "trellis_workspace_bytes", "trellis_gateup_swiglu",
-           "trellis_gemm_prefill", "trellis_device_error")
+           "trellis_gemm_prefill", "trellis_device_error", "trellis_mlp_decode")
 
 
 class TrellisGeom(ctypes.Structure):
@@ -92,6 +92,8 @@ def load(path: str = LIB_PATH):
             lib.trellis_gateup_swiglu.argtypes = [vp, vp, vp, vp, vp, vp, i32, g, vp]
             lib.trellis_gemm_prefill.restype = i32
             lib.trellis_gemm_prefill.argtypes = [vp, vp, vp, vp, i32, g, vp]
+            lib.trellis_mlp_decode.restype = i32
+            lib.trellis_mlp_decode.argtypes = [vp] * 9 + [i32, g, g, vp, sz, vp]
             lib.trellis_device_error.restype = i32
             lib.trellis_device_error.argtypes = [i32]
             _lib = lib
@@ -204,3 +206,55 @@ def gemm_prefill(codes, scales, x, g: Geometry, out=None):
 def device_error(reset: bool = False) -> int:
     """Device error word of the tensor-core kernel (0 = no bounded wait gave up)."""
     return int(load().trellis_device_error(1 if reset else 0))
+
+
+def mlp_decode(gcodes, gscales, ucodes, uscales, dcodes, dscales, x, g_up: Geometry, g_down: Geometry, workspace,
+               hidden=None, out=None):
+    """Decode-time MLP block: out = down(swiglu(gate(x), up(x))), M = 1..4 (two launches)."""
+    M = x.shape[0]
+    if hidden is None:
+        hidden = torch.empty((M, g_up.rows), dtype=torch.bfloat16, device=x.device)
+    if out is None:
+        out = torch.empty((M, g_down.cols), dtype=torch.bfloat16, device=x.device)
+    shp_u, shp_d = (g_up.rows, g_up.words_per_row), (g_down.rows, g_down.words_per_row)
+    args = (_req(gcodes, "gcodes", _CODES, shp_u), _req(gscales, "gscales", (torch.float16,), (g_up.rows,)),
+            _req(ucodes, "ucodes", _CODES, shp_u), _req(uscales, "uscales", (torch.float16,), (g_up.rows,)),
+            _req(dcodes, "dcodes", _CODES, shp_d), _req(dscales, "dscales", (torch.float16,), (g_down.rows,)),
+            _req(x, "x", (torch.bfloat16,), (M, g_up.cols)), _req(hidden, "hidden", (torch.bfloat16,), (M, g_up.rows)),
+            _req(out, "out", (torch.bfloat16,), (M, g_down.cols)))
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    nbytes = workspace.numel() * workspace.element_size()
+    _check("trellis_mlp_decode", load().trellis_mlp_decode(*args, M, ctypes.byref(g_up.c()), ctypes.byref(g_down.c()),
+                                                          workspace.data_ptr(), nbytes, _stream(x)))
+    return hidden, out
+
+
+class MlpDecodeGraph:
+    """The decode MLP block captured once into a CUDA graph and replayed.
+
+    Buffers (x, hidden, out, workspace) are fixed at capture time; write the
+    next token's activations into `x` and call `replay()`.
+    """
+
+    def __init__(self, gcodes, gscales, ucodes, uscales, dcodes, dscales, g_up: Geometry, g_down: Geometry, M: int):
+        dev = gcodes.device
+        self.x = torch.zeros((M, g_up.cols), dtype=torch.bfloat16, device=dev)
+        self.hidden = torch.empty((M, g_up.rows), dtype=torch.bfloat16, device=dev)
+        self.out = torch.empty((M, g_down.cols), dtype=torch.bfloat16, device=dev)
+        self.workspace = new_workspace(M, g_down, dev)
+        self._args = (gcodes, gscales, ucodes, uscales, dcodes, dscales)
+        self._g = (g_up, g_down)
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(s):  # warm-up launch outside the graph (library set-up, first-use costs)
+            mlp_decode(*self._args, self.x, *self._g, self.workspace, self.hidden, self.out)
+        torch.cuda.current_stream(dev).wait_stream(s)
+        torch.cuda.synchronize(dev)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            mlp_decode(*self._args, self.x, *self._g, self.workspace, self.hidden, self.out)
+
+    def replay(self):
+        self.graph.replay()
+        return self.out

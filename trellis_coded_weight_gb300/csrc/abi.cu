@@ -140,6 +140,35 @@ int trellis_gateup_swiglu(const uint32_t* gcodes, const uint16_t* gscales, const
                                                    g->rows, g->cols, static_cast<cudaStream_t>(stream)));
 }
 
+int trellis_mlp_decode(const uint32_t* gcodes, const uint16_t* gscales, const uint32_t* ucodes,
+                       const uint16_t* uscales, const uint32_t* dcodes, const uint16_t* dscales, const uint16_t* x,
+                       uint16_t* hidden, uint16_t* out, int M, const trellis_geom_t* g_up,
+                       const trellis_geom_t* g_down, void* workspace, size_t workspace_bytes,
+                       trellis_stream_t stream) {
+  int st = geom_ok(g_up);
+  if (st) return st;
+  if ((st = geom_ok(g_down))) return st;
+  if (g_up->axis != 1 || g_down->axis != 0) return TRELLIS_EAXIS;
+  if (g_up->rows != g_down->rows || g_up->cols != g_down->cols) return TRELLIS_EGEOM;
+  if (M < 1 || M > 4) return TRELLIS_EM;
+  if (!gcodes || !gscales || !ucodes || !uscales || !dcodes || !dscales || !x || !hidden || !out)
+    return TRELLIS_ENULL;
+  if (!aligned16(gcodes) || !aligned16(gscales) || !aligned16(ucodes) || !aligned16(uscales) ||
+      !aligned16(dcodes) || !aligned16(dscales) || !aligned16(x) || !aligned16(hidden) || !aligned16(out))
+    return TRELLIS_EALIGN;
+  if (!workspace || !aligned16(workspace) ||
+      workspace_bytes < trellis::axis0_workspace_bytes(M, g_down->rows, g_down->cols))
+    return TRELLIS_EWORKSPACE;
+  if ((st = device_ok())) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = trellis::launch_gateup_swiglu(gcodes, gscales, ucodes, uscales, x, hidden, M, g_up->k, g_up->L,
+                                                g_up->rows, g_up->cols, s);
+  if (e != cudaSuccess) return TRELLIS_ECUDA;
+  e = trellis::launch_matvec_axis0(dcodes, dscales, hidden, out, M, g_down->k, g_down->L, g_down->rows,
+                                   g_down->cols, workspace, s);
+  return cuda_status(e);
+}
+
 int trellis_gemm_prefill(const uint32_t* codes, const uint16_t* scales, const uint16_t* x, uint16_t* out, int M,
                          const trellis_geom_t* g, trellis_stream_t stream) {
   int st = geom_ok(g);
