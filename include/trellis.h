@@ -48,12 +48,19 @@ extern "C" {
 /* Geometry of one packed matrix (TrellisGeometry on the "trellis-linear.ts"
  * page: {k, L, T, axis, rows, cols}; rows/cols are the STORED matrix's). */
 typedef struct trellis_geom {
-  int32_t k;     /* bits per weight */
-  int32_t L;     /* window (trellis state) length in bits */
-  int32_t T;     /* positions per block */
-  int32_t axis;  /* 1 or 0, see above */
-  int64_t rows;  /* stored rows */
-  int64_t cols;  /* coded positions per stored row */
+  int32_t k;          /* bits per weight */
+  int32_t L;          /* window (trellis state) length in bits */
+  int32_t T;          /* positions per block */
+  int32_t axis;       /* 1 or 0, see above */
+  int64_t rows;       /* stored rows */
+  int64_t cols;       /* coded positions per stored row */
+  int32_t interleave; /* 0: row-major codes [rows][cols*k/32].
+                         2: the k=3 axis-0 layout [cols/512][rows][48] of the
+                         "trellis-linear.ts" format comment: two coded blocks
+                         of a row side by side (words 0..23 and 24..47), the
+                         rows of one 512-column group contiguous.  Supported
+                         by trellis_expand_bf16 and the axis-0 matvecs. */
+  int32_t reserved;   /* must be 0 */
 } trellis_geom_t;
 
 typedef void *trellis_stream_t; /* a cudaStream_t */
@@ -70,7 +77,7 @@ enum trellis_status {
   TRELLIS_EDEVICE = -8     /* no usable sm_103 device is current */
 };
 
-/* Version of this interface (major*100 + minor). */
+/* Version of this interface (major*100 + minor): 101. */
 int trellis_abi_version(void);
 
 /* Static description of a status code; never NULL. */

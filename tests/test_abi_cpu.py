@@ -109,3 +109,14 @@ def test_mlp_decode_errors_before_launch(lib):
     assert lib.trellis_mlp_decode(*args, 2, ctypes.byref(gd), ctypes.byref(gd), A, need, None) == -4
     assert lib.trellis_mlp_decode(*args, 5, ctypes.byref(gu), ctypes.byref(gd), A, need, None) == -2
     assert lib.trellis_mlp_decode(*args, 2, ctypes.byref(gu), ctypes.byref(gd), A, need - 16, None) == -5
+
+
+@pytest.mark.parametrize("kw,ok", [({"k": 3, "axis": 0, "cols": 1024, "interleave": 2}, True),
+                                   ({"k": 3, "axis": 0, "cols": 1024, "interleave": 2, "L": 12}, True),
+                                   ({"k": 2, "axis": 0, "cols": 1024, "interleave": 2}, False),
+                                   ({"k": 3, "axis": 1, "cols": 1024, "interleave": 2}, False),
+                                   ({"k": 3, "axis": 0, "cols": 768, "interleave": 2}, False),
+                                   ({"k": 3, "axis": 0, "cols": 1024, "interleave": 1}, False),
+                                   ({"reserved": 1}, False)])
+def test_interleaved_geometry_rules(lib, kw, ok):
+    assert (lib.trellis_check_geom(ctypes.byref(G(**kw))) == 0) == ok

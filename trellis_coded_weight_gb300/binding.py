@@ -33,7 +33,8 @@ EXPORTS = ("trellis_abi_version", "trellis_status_string", "trellis_check_geom",
 class TrellisGeom(ctypes.Structure):
     """Mirror of trellis_geom_t."""
     _fields_ = [("k", ctypes.c_int32), ("L", ctypes.c_int32), ("T", ctypes.c_int32), ("axis", ctypes.c_int32),
-                ("rows", ctypes.c_int64), ("cols", ctypes.c_int64)]
+                ("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("interleave", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 @dataclass(frozen=True)
@@ -45,13 +46,20 @@ class Geometry:
     axis: int
     rows: int
     cols: int
+    interleave: int = 0  # 2: the k=3 axis-0 layout [cols/512][rows][48]
 
     def c(self) -> TrellisGeom:
-        return TrellisGeom(self.k, self.L, self.T, self.axis, self.rows, self.cols)
+        return TrellisGeom(self.k, self.L, self.T, self.axis, self.rows, self.cols, self.interleave, 0)
 
     @property
     def words_per_row(self) -> int:
         return self.cols * self.k // 32
+
+    @property
+    def codes_shape(self) -> tuple:
+        if self.interleave:
+            return (self.cols // (2 * self.T), self.rows, 2 * self.T * self.k // 32)
+        return (self.rows, self.words_per_row)
 
 
 class TrellisError(RuntimeError):
@@ -128,7 +136,7 @@ def expand_bf16(codes, scales, g: Geometry, out=None):
     """Decoded stored matrix [rows, cols] bf16 (bit-exact)."""
     if out is None:
         out = torch.empty((g.rows, g.cols), dtype=torch.bfloat16, device=codes.device)
-    args = (_req(codes, "codes", _CODES, (g.rows, g.words_per_row)),
+    args = (_req(codes, "codes", _CODES, g.codes_shape),
             _req(scales, "scales", (torch.float16,), (g.rows,)),
             _req(out, "out", (torch.bfloat16,), (g.rows, g.cols)))
     _check("trellis_expand_bf16", load().trellis_expand_bf16(*args, ctypes.byref(g.c()), _stream(codes)))
@@ -140,7 +148,7 @@ def matvec_axis1(codes, scales, x, g: Geometry, out=None):
     M = x.shape[0]
     if out is None:
         out = torch.empty((M, g.rows), dtype=torch.bfloat16, device=x.device)
-    args = (_req(codes, "codes", _CODES, (g.rows, g.words_per_row)),
+    args = (_req(codes, "codes", _CODES, g.codes_shape),
             _req(scales, "scales", (torch.float16,), (g.rows,)),
             _req(x, "x", (torch.bfloat16,), (M, g.cols)),
             _req(out, "out", (torch.bfloat16,), (M, g.rows)))
@@ -167,7 +175,7 @@ def matvec_axis0(codes, scales, x, g: Geometry, workspace, out=None):
         out = torch.empty((M, g.cols), dtype=torch.bfloat16, device=x.device)
     if not workspace.is_cuda or not workspace.is_contiguous():
         raise ValueError("workspace must be a contiguous CUDA tensor")
-    args = (_req(codes, "codes", _CODES, (g.rows, g.words_per_row)),
+    args = (_req(codes, "codes", _CODES, g.codes_shape),
             _req(scales, "scales", (torch.float16,), (g.rows,)),
             _req(x, "x", (torch.bfloat16,), (M, g.rows)),
             _req(out, "out", (torch.bfloat16,), (M, g.cols)))
@@ -182,7 +190,7 @@ def gateup_swiglu(gcodes, gscales, ucodes, uscales, x, g: Geometry, out=None):
     M = x.shape[0]
     if out is None:
         out = torch.empty((M, g.rows), dtype=torch.bfloat16, device=x.device)
-    shp = (g.rows, g.words_per_row)
+    shp = g.codes_shape
     args = (_req(gcodes, "gcodes", _CODES, shp), _req(gscales, "gscales", (torch.float16,), (g.rows,)),
             _req(ucodes, "ucodes", _CODES, shp), _req(uscales, "uscales", (torch.float16,), (g.rows,)),
             _req(x, "x", (torch.bfloat16,), (M, g.cols)), _req(out, "out", (torch.bfloat16,), (M, g.rows)))
@@ -195,7 +203,7 @@ def gemm_prefill(codes, scales, x, g: Geometry, out=None):
     M = x.shape[0]
     if out is None:
         out = torch.empty((M, g.rows), dtype=torch.bfloat16, device=x.device)
-    args = (_req(codes, "codes", _CODES, (g.rows, g.words_per_row)),
+    args = (_req(codes, "codes", _CODES, g.codes_shape),
             _req(scales, "scales", (torch.float16,), (g.rows,)),
             _req(x, "x", (torch.bfloat16,), (M, g.cols)),
             _req(out, "out", (torch.bfloat16,), (M, g.rows)))
@@ -216,7 +224,7 @@ def mlp_decode(gcodes, gscales, ucodes, uscales, dcodes, dscales, x, g_up: Geome
         hidden = torch.empty((M, g_up.rows), dtype=torch.bfloat16, device=x.device)
     if out is None:
         out = torch.empty((M, g_down.cols), dtype=torch.bfloat16, device=x.device)
-    shp_u, shp_d = (g_up.rows, g_up.words_per_row), (g_down.rows, g_down.words_per_row)
+    shp_u, shp_d = g_up.codes_shape, g_down.codes_shape
     args = (_req(gcodes, "gcodes", _CODES, shp_u), _req(gscales, "gscales", (torch.float16,), (g_up.rows,)),
             _req(ucodes, "ucodes", _CODES, shp_u), _req(uscales, "uscales", (torch.float16,), (g_up.rows,)),
             _req(dcodes, "dcodes", _CODES, shp_d), _req(dscales, "dscales", (torch.float16,), (g_down.rows,)),

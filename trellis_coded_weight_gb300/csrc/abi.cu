@@ -15,7 +15,7 @@
 
 namespace {
 
-constexpr int kAbiVersion = 100;
+constexpr int kAbiVersion = 101;
 constexpr int kMaxDevices = 64;
 // 0 = unknown, 1 = usable sm_103 device, -1 = not usable
 int g_device_ok[kMaxDevices];
@@ -32,6 +32,10 @@ int geom_ok(const trellis_geom_t* g) {
   if (((int64_t)g->T * g->k) % 32 != 0) return TRELLIS_EGEOM;
   if (g->rows > INT32_MAX || g->cols > INT32_MAX || g->rows * g->cols > ((int64_t)1 << 40))
     return TRELLIS_EGEOM;
+  if (g->reserved != 0) return TRELLIS_EGEOM;
+  if (g->interleave != 0) {  // the pages' interleaved layout exists for k = 3, T = 256, axis 0 only
+    if (g->interleave != 2 || g->k != 3 || g->axis != 0 || g->cols % (2 * g->T) != 0) return TRELLIS_EGEOM;
+  }
   return TRELLIS_OK;
 }
 
@@ -85,7 +89,7 @@ int trellis_expand_bf16(const uint32_t* codes, const uint16_t* scales, uint16_t*
   if (!codes || !scales || !out) return TRELLIS_ENULL;
   if (!aligned16(codes) || !aligned16(scales) || !aligned16(out)) return TRELLIS_EALIGN;
   if ((st = device_ok())) return st;
-  return cuda_status(trellis::launch_expand_bf16(codes, scales, out, g->k, g->L, g->rows, g->cols,
+  return cuda_status(trellis::launch_expand_bf16(codes, scales, out, g->k, g->L, g->rows, g->cols, g->interleave,
                                                  static_cast<cudaStream_t>(stream)));
 }
 
@@ -121,7 +125,7 @@ int trellis_matvec_axis0(const uint32_t* codes, const uint16_t* scales, const ui
     return TRELLIS_EWORKSPACE;
   if ((st = device_ok())) return st;
   return cuda_status(trellis::launch_matvec_axis0(codes, scales, x, out, M, g->k, g->L, g->rows, g->cols,
-                                                  workspace, static_cast<cudaStream_t>(stream)));
+                                                  g->interleave, workspace, static_cast<cudaStream_t>(stream)));
 }
 
 int trellis_gateup_swiglu(const uint32_t* gcodes, const uint16_t* gscales, const uint32_t* ucodes,
@@ -165,7 +169,7 @@ int trellis_mlp_decode(const uint32_t* gcodes, const uint16_t* gscales, const ui
                                                 g_up->rows, g_up->cols, s);
   if (e != cudaSuccess) return TRELLIS_ECUDA;
   e = trellis::launch_matvec_axis0(dcodes, dscales, hidden, out, M, g_down->k, g_down->L, g_down->rows,
-                                   g_down->cols, workspace, s);
+                                   g_down->cols, g_down->interleave, workspace, s);
   return cuda_status(e);
 }
 

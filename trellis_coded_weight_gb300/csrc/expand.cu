@@ -30,7 +30,8 @@ constexpr int kExpandThreads = 256;
 template <int K, int L>
 __global__ void __launch_bounds__(kExpandThreads) expand_kernel(const uint32_t* __restrict__ codes,
                                                                const uint16_t* __restrict__ scales,
-                                                               uint16_t* __restrict__ out, int64_t rows, int nb) {
+                                                               uint16_t* __restrict__ out, int64_t rows, int nb,
+                                                               int interleave) {
   constexpr int WPB = kT * K / 32;
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = (int64_t)gridDim.x * (kExpandThreads / 32);
@@ -42,10 +43,17 @@ __global__ void __launch_bounds__(kExpandThreads) expand_kernel(const uint32_t* 
   const int wb = (wa + 1 == WPB) ? 0 : wa + 1;
   const float2 nmagic = make_float2(-kMagic, -kMagic);
 
+  // block (row, blk) of item i: row-major, or the interleaved [nb/2][rows][2*WPB] layout
+  auto block_of = [&](int64_t i) -> const uint32_t* {
+    if (!interleave) return codes + i * WPB;
+    const int64_t row = i / nb;
+    const int blk = (int)(i - row * nb);
+    return codes + ((int64_t)(blk >> 1) * rows + row) * (2 * WPB) + (blk & 1) * WPB;
+  };
   uint32_t a = 0, b = 0;
   uint16_t sc16 = 0;
   if (it < items) {
-    const uint32_t* bw = codes + it * WPB;
+    const uint32_t* bw = block_of(it);
     a = __ldg(bw + wa);
     b = __ldg(bw + wb);
     sc16 = __ldg(scales + it / nb);
@@ -56,7 +64,7 @@ __global__ void __launch_bounds__(kExpandThreads) expand_kernel(const uint32_t* 
     uint32_t na = 0, nbw = 0;
     uint16_t nsc = 0;
     if (nx < items) {
-      const uint32_t* bw = codes + nx * WPB;
+      const uint32_t* bw = block_of(nx);
       na = __ldg(bw + wa);
       nbw = __ldg(bw + wb);
       nsc = __ldg(scales + nx / nb);
@@ -83,7 +91,7 @@ __global__ void __launch_bounds__(kExpandThreads) expand_kernel(const uint32_t* 
 }
 
 cudaError_t launch_expand_bf16(const uint32_t* codes, const uint16_t* scales, uint16_t* out, int k, int L,
-                               int64_t rows, int64_t cols, cudaStream_t st) {
+                               int64_t rows, int64_t cols, int interleave, cudaStream_t st) {
   const int nb = (int)(cols / kT);
   const int64_t warps = rows * nb;
   int dev = 0, sms = 148;
@@ -92,13 +100,13 @@ cudaError_t launch_expand_bf16(const uint32_t* codes, const uint16_t* scales, ui
   if (nblk > (int64_t)sms * 8) nblk = (int64_t)sms * 8;  // eight 256-thread CTAs per SM, grid-stride
   const dim3 block(kExpandThreads), grid((unsigned)nblk);
   if (L == 16) {
-    if (k == 2) expand_kernel<2, 16><<<grid, block, 0, st>>>(codes, scales, out, rows, nb);
-    else if (k == 3) expand_kernel<3, 16><<<grid, block, 0, st>>>(codes, scales, out, rows, nb);
-    else expand_kernel<4, 16><<<grid, block, 0, st>>>(codes, scales, out, rows, nb);
+    if (k == 2) expand_kernel<2, 16><<<grid, block, 0, st>>>(codes, scales, out, rows, nb, interleave);
+    else if (k == 3) expand_kernel<3, 16><<<grid, block, 0, st>>>(codes, scales, out, rows, nb, interleave);
+    else expand_kernel<4, 16><<<grid, block, 0, st>>>(codes, scales, out, rows, nb, interleave);
   } else {
-    if (k == 2) expand_kernel<2, 12><<<grid, block, 0, st>>>(codes, scales, out, rows, nb);
-    else if (k == 3) expand_kernel<3, 12><<<grid, block, 0, st>>>(codes, scales, out, rows, nb);
-    else expand_kernel<4, 12><<<grid, block, 0, st>>>(codes, scales, out, rows, nb);
+    if (k == 2) expand_kernel<2, 12><<<grid, block, 0, st>>>(codes, scales, out, rows, nb, interleave);
+    else if (k == 3) expand_kernel<3, 12><<<grid, block, 0, st>>>(codes, scales, out, rows, nb, interleave);
+    else expand_kernel<4, 12><<<grid, block, 0, st>>>(codes, scales, out, rows, nb, interleave);
   }
   return cudaGetLastError();
 }

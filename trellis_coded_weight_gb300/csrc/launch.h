@@ -10,8 +10,9 @@ namespace trellis {
 
 constexpr int kT_host = 256;  // positions per block, the only T the kernels support
 
+// interleave: 0 row-major codes, 2 the k=3 axis-0 layout [cols/512][rows][48].
 cudaError_t launch_expand_bf16(const uint32_t* codes, const uint16_t* scales, uint16_t* out, int k, int L,
-                               int64_t rows, int64_t cols, cudaStream_t st);
+                               int64_t rows, int64_t cols, int interleave, cudaStream_t st);
 
 cudaError_t launch_matvec_axis1(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
                                 uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols,
@@ -25,7 +26,7 @@ cudaError_t launch_gateup_swiglu(const uint32_t* gcodes, const uint16_t* gscales
 // arrival counters.
 size_t axis0_workspace_bytes(int M, int64_t rows, int64_t cols);
 cudaError_t launch_matvec_axis0(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
-                                uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols,
+                                uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols, int interleave,
                                 void* workspace, cudaStream_t st);
 
 cudaError_t launch_gemm_prefill(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,

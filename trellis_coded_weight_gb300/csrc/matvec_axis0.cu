@@ -66,6 +66,7 @@ struct Ax0Params {
   uint32_t* counter;  // [nb]
   int64_t R, C, rps;
   int nb, S;
+  int interleave;  // 2: codes in the [nb/2][R][2*WPB] layout
 };
 
 template <int K, int L, int M>
@@ -92,8 +93,10 @@ __global__ void __launch_bounds__(32 * kAx0Warps) ax0_kernel(const Ax0Params p) 
   const int lo = (kT - 8 * (lane + 1)) * K;
   const int wa = lo >> 5, sh = lo & 31;
   const int wb = (wa + 1 == WPB) ? 0 : wa + 1;
-  const int64_t rowWords = (int64_t)p.nb * WPB;
-  const uint32_t* base = p.codes + (int64_t)cb * WPB;
+  // row stride and first word of column block cb in either layout
+  const int64_t rowWords = p.interleave ? 2 * WPB : (int64_t)p.nb * WPB;
+  const uint32_t* base = p.interleave ? p.codes + (int64_t)(cb >> 1) * p.R * (2 * WPB) + (cb & 1) * WPB
+                                      : p.codes + (int64_t)cb * WPB;
   const float2 nmagic = make_float2(-kMagic, -kMagic);
 
   float2 acc[M][4];
@@ -206,7 +209,7 @@ static cudaError_t ax0_launch_m(const Ax0Params& p, int M, cudaStream_t st) {
 }
 
 cudaError_t launch_matvec_axis0(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
-                                uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols,
+                                uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols, int interleave,
                                 void* workspace, cudaStream_t st) {
   const Ax0Plan pl = ax0_plan(rows, cols);
   Ax0Params p{};
@@ -214,7 +217,7 @@ cudaError_t launch_matvec_axis0(const uint32_t* codes, const uint16_t* scales, c
   p.part = static_cast<float*>(workspace);
   p.counter = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) +
                                           (size_t)pl.S * (size_t)M * (size_t)cols * sizeof(float));
-  p.R = rows; p.C = cols; p.rps = pl.rps; p.nb = pl.nb; p.S = pl.S;
+  p.R = rows; p.C = cols; p.rps = pl.rps; p.nb = pl.nb; p.S = pl.S; p.interleave = interleave;
   if (L == 16) {
     if (k == 2) return ax0_launch_m<2, 16>(p, M, st);
     if (k == 3) return ax0_launch_m<3, 16>(p, M, st);

@@ -86,6 +86,6 @@ extern "C" int trellis_matvec_axis0_noalloc(const uint32_t* codes, const uint16_
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(static_cast<char*>(ws) + counters, 0, need - counters, s) != cudaSuccess) return TRELLIS_ECUDA;
   const cudaError_t e =
-      trellis::launch_matvec_axis0(codes, scales, x, out, M, g->k, g->L, g->rows, g->cols, ws, s);
+      trellis::launch_matvec_axis0(codes, scales, x, out, M, g->k, g->L, g->rows, g->cols, g->interleave, ws, s);
   return e == cudaSuccess ? TRELLIS_OK : TRELLIS_ECUDA;
 }
