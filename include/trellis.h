@@ -133,6 +133,20 @@ int trellis_matvec_axis0(const uint32_t *codes, const uint16_t *scales, const ui
                          uint16_t *out, int M, const trellis_geom_t *g, void *workspace,
                          size_t workspace_bytes, trellis_stream_t stream);
 
+/*
+ * trellis_matvec_axis1_bf16w, trellis_matvec_axis0_bf16w -- the two matvecs
+ * with the pages' bf16-rounded weight numerics (decoder variants 0-3 of the
+ * HEADER source in "trellis-linear.ts", TRELLIS_ROUND): every weight is
+ * bf16(fl32(value * scale)) with the correctly rounded value -- exactly the
+ * trellis_expand_bf16 weight -- before the fp32 multiply-add.  Arguments,
+ * shapes, workspace and errors as for trellis_matvec_axis1 / _axis0.
+ */
+int trellis_matvec_axis1_bf16w(const uint32_t *codes, const uint16_t *scales, const uint16_t *x,
+                               uint16_t *out, int M, const trellis_geom_t *g, trellis_stream_t stream);
+int trellis_matvec_axis0_bf16w(const uint32_t *codes, const uint16_t *scales, const uint16_t *x,
+                               uint16_t *out, int M, const trellis_geom_t *g, void *workspace,
+                               size_t workspace_bytes, trellis_stream_t stream);
+
 /* Bytes of workspace trellis_matvec_axis0 needs for (M, g); 0 if the
  * geometry or M is unsupported. */
 size_t trellis_workspace_bytes(int M, const trellis_geom_t *g);

@@ -72,6 +72,8 @@ def _load():
                                            _P_I64, _I64, _P_F64, _P_F64]),
                 "or_matvec_axis0": (None, [_P_U32, _P_U16, _P_U16, _INT, _INT, _INT, _INT, _I64, _I64,
                                            _P_I64, _I64, _P_F64, _P_F64]),
+                "or_matvec_axis0_bf16w": (None, [_P_U32, _P_U16, _P_U16, _INT, _INT, _INT, _INT, _I64, _I64,
+                                                 _P_I64, _I64, _P_F64, _P_F64]),
                 "or_swiglu_bf16": (ctypes.c_uint16, [ctypes.c_uint16, ctypes.c_uint16]),
                 "or_swiglu_bf16_many": (None, [_P_U16, _P_U16, _P_U16, _I64]),
                 "or_gateup_sums": (None, [_P_U32, _P_U16, _P_U32, _P_U16, _P_U16, _INT, _INT, _INT, _INT,
@@ -215,6 +217,17 @@ def matvec_axis0(codes, scales, x, k, L, T, cols=None):
     """(ref, absum) [M, n]: out[m, c] = sum_r w(r,c) x[m,r] in double (stored W^T)."""
     assert np.shape(x)[1] == np.shape(codes)[0]
     return _mv(_load().or_matvec_axis0, codes, scales, x, k, L, T, cols, lambda R, C: C)
+
+
+def matvec_axis0_bf16w(codes, scales, x, k, L, T, cols=None):
+    """Axis-0 matvec with bf16-rounded weights (the expand weights), in double."""
+    assert np.shape(x)[1] == np.shape(codes)[0]
+    return _mv(_load().or_matvec_axis0_bf16w, codes, scales, x, k, L, T, cols, lambda R, C: C)
+
+
+def matvec_axis1_bf16w(codes, scales, x, k, L, T, rows=None):
+    """Axis-1 matvec with bf16-rounded weights: the same sum as prefill()."""
+    return prefill(codes, scales, x, k, L, T, rows)
 
 
 def prefill(codes, scales, x, k, L, T, rows=None):

@@ -268,6 +268,31 @@ void or_matvec_axis0(const uint32_t *codes, const uint16_t *scales, const uint16
   free(w);
 }
 
+/* Axis-0 matvec with the bf16-rounded weight numerics (decoder variants 0-3
+ * of the HEADER source): w = bf16(fl32(value * scale)), the expand weight. */
+void or_matvec_axis0_bf16w(const uint32_t *codes, const uint16_t *scales, const uint16_t *x, int M, int k,
+                           int L, int T, int64_t rows, int64_t cols, const int64_t *col_idx, int64_t n_cols,
+                           double *ref, double *absum) {
+  double *w = (double *)malloc(sizeof(double) * (size_t)rows);
+  if (!w) return;
+  for (int64_t j = 0; j < n_cols; ++j) {
+    const int64_t c = col_idx[j];
+    for (int64_t r = 0; r < rows; ++r)
+      w[r] = (double)or_bf16_to_f32(or_bf16_rne(entry_weight_f32(codes, scales, T, k, L, cols, r, c)));
+    for (int m = 0; m < M; ++m) {
+      double acc = 0.0, aacc = 0.0;
+      for (int64_t r = 0; r < rows; ++r) {
+        const double p = w[r] * (double)or_bf16_to_f32(x[(int64_t)m * rows + r]);
+        acc += p;
+        aacc += fabs(p);
+      }
+      ref[(int64_t)m * n_cols + j] = acc;
+      absum[(int64_t)m * n_cols + j] = aacc;
+    }
+  }
+  free(w);
+}
+
 /* ---------- fused gate/up SwiGLU ---------------------------------------- */
 
 /* The activation chain on bf16 gate and up values, evaluated in fp32 with

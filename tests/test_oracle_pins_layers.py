@@ -206,3 +206,15 @@ def test_prefill_equals_expand_then_matmul(oracle_mod):
     assert np.allclose(ref, want, rtol=0, atol=1e-12 * ab.max())
     part, _ = oracle_mod.prefill(codes, scales, x, 2, 16, 256, rows=[19, 4])
     assert np.array_equal(part, ref[:, [19, 4]])
+
+
+@pytest.mark.parametrize("k", [2, 3])
+def test_matvec_axis0_bf16w_equals_expand_then_gemv(oracle_mod, k):
+    """Variants 0-3 (TRELLIS_ROUND): weights are the bf16 expand weights;
+    against numpy's float64 x @ E for the stored W^T."""
+    rows, cols = 33, 512
+    codes, scales, x = inputs.make_linear(rows, cols, k, 3, seed_codes=12, sigma=0.5, x_len=rows)
+    e = inputs.bf16_bits_to_f32(oracle_mod.expand_bf16(codes, scales, k, 16, 256)).astype(np.float64)
+    ref, ab = oracle_mod.matvec_axis0_bf16w(codes, scales, x, k, 16, 256)
+    want = inputs.bf16_bits_to_f32(x).astype(np.float64) @ e
+    assert np.allclose(ref, want, rtol=0, atol=1e-12 * ab.max())

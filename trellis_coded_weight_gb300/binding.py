@@ -27,7 +27,8 @@ STATUS_NAMES = {0: "TRELLIS_OK", -1: "TRELLIS_EGEOM", -2: "TRELLIS_EM", -3: "TRE
 
 EXPORTS = ("trellis_abi_version", "trellis_status_string", "trellis_check_geom", "trellis_expand_bf16",
            "trellis_matvec_axis1", "trellis_matvec_axis0", "trellis_workspace_bytes", "trellis_gateup_swiglu",
-           "trellis_gemm_prefill", "trellis_device_error", "trellis_mlp_decode")
+           "trellis_gemm_prefill", "trellis_device_error", "trellis_mlp_decode", "trellis_matvec_axis1_bf16w",
+           "trellis_matvec_axis0_bf16w")
 
 
 class TrellisGeom(ctypes.Structure):
@@ -100,6 +101,10 @@ def load(path: str = LIB_PATH):
             lib.trellis_gateup_swiglu.argtypes = [vp, vp, vp, vp, vp, vp, i32, g, vp]
             lib.trellis_gemm_prefill.restype = i32
             lib.trellis_gemm_prefill.argtypes = [vp, vp, vp, vp, i32, g, vp]
+            lib.trellis_matvec_axis1_bf16w.restype = i32
+            lib.trellis_matvec_axis1_bf16w.argtypes = [vp, vp, vp, vp, i32, g, vp]
+            lib.trellis_matvec_axis0_bf16w.restype = i32
+            lib.trellis_matvec_axis0_bf16w.argtypes = [vp, vp, vp, vp, i32, g, vp, sz, vp]
             lib.trellis_mlp_decode.restype = i32
             lib.trellis_mlp_decode.argtypes = [vp] * 9 + [i32, g, g, vp, sz, vp]
             lib.trellis_device_error.restype = i32
@@ -143,8 +148,10 @@ def expand_bf16(codes, scales, g: Geometry, out=None):
     return out
 
 
-def matvec_axis1(codes, scales, x, g: Geometry, out=None):
-    """out[M, rows] = x[M, cols] @ W^T for an axis-1 matrix, M = 1..4."""
+def matvec_axis1(codes, scales, x, g: Geometry, out=None, bf16_weights: bool = False):
+    """out[M, rows] = x[M, cols] @ W^T for an axis-1 matrix, M = 1..4.
+
+    bf16_weights selects the bf16-rounded weight numerics (the expand weights)."""
     M = x.shape[0]
     if out is None:
         out = torch.empty((M, g.rows), dtype=torch.bfloat16, device=x.device)
@@ -152,7 +159,8 @@ def matvec_axis1(codes, scales, x, g: Geometry, out=None):
             _req(scales, "scales", (torch.float16,), (g.rows,)),
             _req(x, "x", (torch.bfloat16,), (M, g.cols)),
             _req(out, "out", (torch.bfloat16,), (M, g.rows)))
-    _check("trellis_matvec_axis1", load().trellis_matvec_axis1(*args, M, ctypes.byref(g.c()), _stream(x)))
+    fn = "trellis_matvec_axis1_bf16w" if bf16_weights else "trellis_matvec_axis1"
+    _check(fn, getattr(load(), fn)(*args, M, ctypes.byref(g.c()), _stream(x)))
     return out
 
 
@@ -168,8 +176,10 @@ def new_workspace(M: int, g: Geometry, device) -> torch.Tensor:
     return torch.zeros(((n + 15) // 16) * 4, dtype=torch.int32, device=device)
 
 
-def matvec_axis0(codes, scales, x, g: Geometry, workspace, out=None):
-    """out[M, cols] = x[M, rows] @ W^T for an axis-0 matrix (stored W^T), M = 1..4."""
+def matvec_axis0(codes, scales, x, g: Geometry, workspace, out=None, bf16_weights: bool = False):
+    """out[M, cols] = x[M, rows] @ W^T for an axis-0 matrix (stored W^T), M = 1..4.
+
+    bf16_weights selects the bf16-rounded weight numerics (the expand weights)."""
     M = x.shape[0]
     if out is None:
         out = torch.empty((M, g.cols), dtype=torch.bfloat16, device=x.device)
@@ -180,8 +190,8 @@ def matvec_axis0(codes, scales, x, g: Geometry, workspace, out=None):
             _req(x, "x", (torch.bfloat16,), (M, g.rows)),
             _req(out, "out", (torch.bfloat16,), (M, g.cols)))
     nbytes = workspace.numel() * workspace.element_size()
-    _check("trellis_matvec_axis0", load().trellis_matvec_axis0(*args, M, ctypes.byref(g.c()), workspace.data_ptr(),
-                                                              nbytes, _stream(x)))
+    fn = "trellis_matvec_axis0_bf16w" if bf16_weights else "trellis_matvec_axis0"
+    _check(fn, getattr(load(), fn)(*args, M, ctypes.byref(g.c()), workspace.data_ptr(), nbytes, _stream(x)))
     return out
 
 

@@ -106,6 +106,36 @@ int trellis_matvec_axis1(const uint32_t* codes, const uint16_t* scales, const ui
                                                   static_cast<cudaStream_t>(stream)));
 }
 
+int trellis_matvec_axis1_bf16w(const uint32_t* codes, const uint16_t* scales, const uint16_t* x, uint16_t* out,
+                               int M, const trellis_geom_t* g, trellis_stream_t stream) {
+  int st = geom_ok(g);
+  if (st) return st;
+  if (g->axis != 1) return TRELLIS_EAXIS;
+  if (M < 1 || M > 4) return TRELLIS_EM;
+  if (!codes || !scales || !x || !out) return TRELLIS_ENULL;
+  if (!aligned16(codes) || !aligned16(scales) || !aligned16(x) || !aligned16(out)) return TRELLIS_EALIGN;
+  if ((st = device_ok())) return st;
+  return cuda_status(trellis::launch_matvec_axis1_bf16w(codes, scales, x, out, M, g->k, g->L, g->rows, g->cols,
+                                                        static_cast<cudaStream_t>(stream)));
+}
+
+int trellis_matvec_axis0_bf16w(const uint32_t* codes, const uint16_t* scales, const uint16_t* x, uint16_t* out,
+                               int M, const trellis_geom_t* g, void* workspace, size_t workspace_bytes,
+                               trellis_stream_t stream) {
+  int st = geom_ok(g);
+  if (st) return st;
+  if (g->axis != 0) return TRELLIS_EAXIS;
+  if (M < 1 || M > 4) return TRELLIS_EM;
+  if (!codes || !scales || !x || !out) return TRELLIS_ENULL;
+  if (!aligned16(codes) || !aligned16(scales) || !aligned16(x) || !aligned16(out)) return TRELLIS_EALIGN;
+  if (!workspace || !aligned16(workspace) ||
+      workspace_bytes < trellis::axis0_workspace_bytes(M, g->rows, g->cols))
+    return TRELLIS_EWORKSPACE;
+  if ((st = device_ok())) return st;
+  return cuda_status(trellis::launch_matvec_axis0_bf16w(codes, scales, x, out, M, g->k, g->L, g->rows, g->cols,
+                                                        g->interleave, workspace, static_cast<cudaStream_t>(stream)));
+}
+
 size_t trellis_workspace_bytes(int M, const trellis_geom_t* g) {
   if (geom_ok(g) != TRELLIS_OK || M < 1 || M > 4) return 0;
   return trellis::axis0_workspace_bytes(M, g->rows, g->cols);

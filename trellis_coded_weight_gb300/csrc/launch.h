@@ -18,6 +18,14 @@ cudaError_t launch_matvec_axis1(const uint32_t* codes, const uint16_t* scales, c
                                 uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols,
                                 cudaStream_t st);
 
+// The same matvecs with bf16-rounded weights (bf16(value * scale) before the FMA).
+cudaError_t launch_matvec_axis1_bf16w(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
+                                      uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols,
+                                      cudaStream_t st);
+cudaError_t launch_matvec_axis0_bf16w(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
+                                      uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols, int interleave,
+                                      void* workspace, cudaStream_t st);
+
 cudaError_t launch_gateup_swiglu(const uint32_t* gcodes, const uint16_t* gscales, const uint32_t* ucodes,
                                  const uint16_t* uscales, const uint16_t* x, uint16_t* out, int M, int k,
                                  int L, int64_t rows, int64_t cols, cudaStream_t st);

@@ -45,7 +45,7 @@ static Ax0Plan ax0_plan(int64_t rows, int64_t cols) {
   p.nb = (int)(cols / kT);
   int64_t rps = (rows * p.nb + kAx0TargetCtas - 1) / kAx0TargetCtas;
   if (rps < 32) rps = 32;
-  if (rps > 2000) rps = 2000;  // keeps the staged x*scale slice within 48 KB of shared memory
+  if (rps > 1600) rps = 1600;  // keeps the staged slice (and its scales) within 48 KB of shared memory
   p.S = (int)((rows + rps - 1) / rps);
   p.rps = (rows + p.S - 1) / p.S;
   return p;
@@ -69,12 +69,13 @@ struct Ax0Params {
   int interleave;  // 2: codes in the [nb/2][R][2*WPB] layout
 };
 
-template <int K, int L, int M>
+template <int K, int L, int M, bool BW>
 __global__ void __launch_bounds__(32 * kAx0Warps) ax0_kernel(const Ax0Params p) {
   constexpr int WPB = kT * K / 32;
   extern __shared__ __align__(16) float smem[];
   float* xs = smem;                        // [rps][M]  x*scale of this slice's rows
   float* red = smem + ((p.rps * M + 3) & ~(int64_t)3);  // [warps][M][256], 16-byte aligned
+  float* scs = red + kAx0Warps * M * kT;                 // [rps] row scales (bf16-weight numerics)
   __shared__ uint32_t last_flag;
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -86,8 +87,12 @@ __global__ void __launch_bounds__(32 * kAx0Warps) ax0_kernel(const Ax0Params p) 
   for (int i = threadIdx.x; i < nr * M; i += blockDim.x) {
     const int rl = i / M, m = i - rl * M;
     const int64_t r = r0 + rl;
-    xs[i] = __fmul_rn(bf16_to_f32(__ldg(p.x + (int64_t)m * p.R + r)), f16_to_f32(__ldg(p.scales + r)));
+    const float xv = bf16_to_f32(__ldg(p.x + (int64_t)m * p.R + r));
+    // default numerics fold the row scale into x; bf16 weights need it per weight
+    xs[i] = BW ? xv : __fmul_rn(xv, f16_to_f32(__ldg(p.scales + r)));
   }
+  if (BW)
+    for (int i = threadIdx.x; i < nr; i += blockDim.x) scs[i] = f16_to_f32(__ldg(p.scales + r0 + i));
   __syncthreads();
 
   const int lo = (kT - 8 * (lane + 1)) * K;
@@ -121,8 +126,14 @@ __global__ void __launch_bounds__(32 * kAx0Warps) ax0_kernel(const Ax0Params p) 
     for (int i2 = 0; i2 < 4; ++i2) {
       const uint32_t s0 = window_at<L, 2>(w, (7 - 2 * i2) * K);
       const uint32_t s1 = window_at<L, 2>(w, (6 - 2 * i2) * K);
-      const float2 y = __fadd2_rn(make_float2(__uint_as_float(code_magic(s0)), __uint_as_float(code_magic(s1))),
-                                  nmagic);
+      float2 y = __fadd2_rn(make_float2(__uint_as_float(code_magic(s0)), __uint_as_float(code_magic(s1))),
+                            nmagic);
+      if constexpr (BW) {  // bf16(value * scale), the expand weight
+        const float sr = scs[rl];
+        const float2 w = __fmul2_rn(value_rn2(y), make_float2(sr, sr));
+        const uint32_t bb = pack_bf16x2(w.x, w.y);
+        y = make_float2(bf16lo_to_f32(bb), bf16hi_to_f32(bb));
+      }
 #pragma unroll
       for (int m = 0; m < M; ++m) acc[m][i2] = __ffma2_rn(y, make_float2(xr[m], xr[m]), acc[m][i2]);
     }
@@ -189,28 +200,30 @@ __global__ void __launch_bounds__(32 * kAx0Warps) ax0_kernel(const Ax0Params p) 
     float v = 0.f;
     for (int s = 0; s < p.S; ++s) v += __ldcg(p.part + ((int64_t)s * M + m) * p.C + (int64_t)cb * kT + t);
     uint16_t o;
-    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(o) : "f"(__fmul_rn(v, kRcpD)));
+    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(o) : "f"(BW ? v : __fmul_rn(v, kRcpD)));
     p.out[(int64_t)m * p.C + (int64_t)cb * kT + t] = o;
   }
   if (threadIdx.x == 0) p.counter[cb] = 0u;
 }
 
-template <int K, int L>
+template <int K, int L, bool BW>
 static cudaError_t ax0_launch_m(const Ax0Params& p, int M, cudaStream_t st) {
   const dim3 grid((unsigned)p.nb, (unsigned)p.S), block(32 * kAx0Warps);
-  const size_t sm = ((((size_t)p.rps * M + 3) & ~(size_t)3) + (size_t)kAx0Warps * M * kT) * sizeof(float);
+  const size_t sm = ((((size_t)p.rps * M + 3) & ~(size_t)3) + (size_t)kAx0Warps * M * kT + (BW ? (size_t)p.rps : 0)) *
+                    sizeof(float);
   switch (M) {
-    case 1: ax0_kernel<K, L, 1><<<grid, block, sm, st>>>(p); break;
-    case 2: ax0_kernel<K, L, 2><<<grid, block, sm, st>>>(p); break;
-    case 3: ax0_kernel<K, L, 3><<<grid, block, sm, st>>>(p); break;
-    default: ax0_kernel<K, L, 4><<<grid, block, sm, st>>>(p); break;
+    case 1: ax0_kernel<K, L, 1, BW><<<grid, block, sm, st>>>(p); break;
+    case 2: ax0_kernel<K, L, 2, BW><<<grid, block, sm, st>>>(p); break;
+    case 3: ax0_kernel<K, L, 3, BW><<<grid, block, sm, st>>>(p); break;
+    default: ax0_kernel<K, L, 4, BW><<<grid, block, sm, st>>>(p); break;
   }
   return cudaGetLastError();
 }
 
-cudaError_t launch_matvec_axis0(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
-                                uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols, int interleave,
-                                void* workspace, cudaStream_t st) {
+template <bool BW>
+static cudaError_t ax0_dispatch(const uint32_t* codes, const uint16_t* scales, const uint16_t* x, uint16_t* out, int M,
+                                int k, int L, int64_t rows, int64_t cols, int interleave, void* workspace,
+                                cudaStream_t st) {
   const Ax0Plan pl = ax0_plan(rows, cols);
   Ax0Params p{};
   p.codes = codes; p.scales = scales; p.x = x; p.out = out;
@@ -219,13 +232,25 @@ cudaError_t launch_matvec_axis0(const uint32_t* codes, const uint16_t* scales, c
                                           (size_t)pl.S * (size_t)M * (size_t)cols * sizeof(float));
   p.R = rows; p.C = cols; p.rps = pl.rps; p.nb = pl.nb; p.S = pl.S; p.interleave = interleave;
   if (L == 16) {
-    if (k == 2) return ax0_launch_m<2, 16>(p, M, st);
-    if (k == 3) return ax0_launch_m<3, 16>(p, M, st);
-    return ax0_launch_m<4, 16>(p, M, st);
+    if (k == 2) return ax0_launch_m<2, 16, BW>(p, M, st);
+    if (k == 3) return ax0_launch_m<3, 16, BW>(p, M, st);
+    return ax0_launch_m<4, 16, BW>(p, M, st);
   }
-  if (k == 2) return ax0_launch_m<2, 12>(p, M, st);
-  if (k == 3) return ax0_launch_m<3, 12>(p, M, st);
-  return ax0_launch_m<4, 12>(p, M, st);
+  if (k == 2) return ax0_launch_m<2, 12, BW>(p, M, st);
+  if (k == 3) return ax0_launch_m<3, 12, BW>(p, M, st);
+  return ax0_launch_m<4, 12, BW>(p, M, st);
+}
+
+cudaError_t launch_matvec_axis0(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
+                                uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols, int interleave,
+                                void* workspace, cudaStream_t st) {
+  return ax0_dispatch<false>(codes, scales, x, out, M, k, L, rows, cols, interleave, workspace, st);
+}
+
+cudaError_t launch_matvec_axis0_bf16w(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
+                                      uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols, int interleave,
+                                      void* workspace, cudaStream_t st) {
+  return ax0_dispatch<true>(codes, scales, x, out, M, k, L, rows, cols, interleave, workspace, st);
 }
 
 }  // namespace trellis

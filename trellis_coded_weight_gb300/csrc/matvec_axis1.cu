@@ -82,7 +82,7 @@ __device__ __forceinline__ void load_half(HalfBlock<K, NMAT>& hbk, const uint32_
   }
 }
 
-template <int K, int L, int M, bool GU>
+template <int K, int L, int M, bool GU, bool BW>
 __global__ void __launch_bounds__(512) mv1_kernel(const Mv1Params p) {
   extern __shared__ __align__(16) float smem[];
   constexpr int NMAT = GU ? 2 : 1;
@@ -107,6 +107,15 @@ __global__ void __launch_bounds__(512) mv1_kernel(const Mv1Params p) {
 #pragma unroll
     for (int m = 0; m < M; ++m) acc[t][m][0] = acc[t][m][1] = make_float2(0.f, 0.f);
   const float2 nmagic = make_float2(-kMagic, -kMagic);
+  // bf16-weight numerics: each weight is bf16(value * scale) before the FMA
+  float wsc[NMAT];
+#pragma unroll
+  for (int t = 0; t < NMAT; ++t) wsc[t] = BW ? f16_to_f32(__ldg(p.scales[t] + rr)) : 1.0f;
+  auto bf16_weights = [&](float2 y, float sc) -> float2 {
+    const float2 w = __fmul2_rn(value_rn2(y), make_float2(sc, sc));
+    const uint32_t b = pack_bf16x2(w.x, w.y);
+    return make_float2(bf16lo_to_f32(b), bf16hi_to_f32(b));
+  };
 
   auto process = [&](const HalfBlock<K, NMAT>& hbk, int ci) {
     const int b = ci >> 1, hb = ci & 1;
@@ -133,10 +142,14 @@ __global__ void __launch_bounds__(512) mv1_kernel(const Mv1Params p) {
         run_states<K, L>(w, s);
 #pragma unroll
         for (int j4 = 0; j4 < 8; ++j4) {
-          const float2 ya = __fadd2_rn(make_float2(__uint_as_float(code_magic(s[4 * j4])),
-                                                   __uint_as_float(code_magic(s[4 * j4 + 1]))), nmagic);
-          const float2 yb = __fadd2_rn(make_float2(__uint_as_float(code_magic(s[4 * j4 + 2])),
-                                                   __uint_as_float(code_magic(s[4 * j4 + 3]))), nmagic);
+          float2 ya = __fadd2_rn(make_float2(__uint_as_float(code_magic(s[4 * j4])),
+                                             __uint_as_float(code_magic(s[4 * j4 + 1]))), nmagic);
+          float2 yb = __fadd2_rn(make_float2(__uint_as_float(code_magic(s[4 * j4 + 2])),
+                                             __uint_as_float(code_magic(s[4 * j4 + 3]))), nmagic);
+          if constexpr (BW) {
+            ya = bf16_weights(ya, wsc[t]);
+            yb = bf16_weights(yb, wsc[t]);
+          }
 #pragma unroll
           for (int m = 0; m < M; ++m) {
             const float4 xv = *reinterpret_cast<const float4*>(xs + m * HB + xq + 4 * j4);
@@ -168,7 +181,7 @@ __global__ void __launch_bounds__(512) mv1_kernel(const Mv1Params p) {
   if (warp != 0 || row >= p.R) return;
   float f[NMAT];
 #pragma unroll
-  for (int t = 0; t < NMAT; ++t) f[t] = __fmul_rn(f16_to_f32(p.scales[t][row]), kRcpD);
+  for (int t = 0; t < NMAT; ++t) f[t] = BW ? 1.0f : __fmul_rn(f16_to_f32(p.scales[t][row]), kRcpD);
 #pragma unroll
   for (int m = 0; m < M; ++m) {
     float v[NMAT];
@@ -196,42 +209,42 @@ static int mv1_splits(int nb, int regs) {
   return s < 1 ? 1 : s;
 }
 
-template <int K, int L, int M, bool GU>
+template <int K, int L, int M, bool GU, bool BW>
 static cudaError_t mv1_launch(const Mv1Params& p, cudaStream_t st) {
   static int regs = 0;  // per instantiation
   if (!regs) {
     cudaFuncAttributes a;
-    if (cudaFuncGetAttributes(&a, mv1_kernel<K, L, M, GU>) != cudaSuccess) return cudaGetLastError();
+    if (cudaFuncGetAttributes(&a, mv1_kernel<K, L, M, GU, BW>) != cudaSuccess) return cudaGetLastError();
     regs = a.numRegs;
   }
   const int S = mv1_splits(p.nb, regs);
   const int nmat = GU ? 2 : 1;
   const size_t sm = (size_t)S * M * (kT / 2) * sizeof(float) + (size_t)nmat * S * M * 32 * sizeof(float);
   const dim3 grid((unsigned)((p.R + 31) / 32)), block(32 * S);
-  mv1_kernel<K, L, M, GU><<<grid, block, sm, st>>>(p);
+  mv1_kernel<K, L, M, GU, BW><<<grid, block, sm, st>>>(p);
   return cudaGetLastError();
 }
 
-template <int K, int L, bool GU>
+template <int K, int L, bool GU, bool BW>
 static cudaError_t mv1_launch_m(const Mv1Params& p, int M, cudaStream_t st) {
   switch (M) {
-    case 1: return mv1_launch<K, L, 1, GU>(p, st);
-    case 2: return mv1_launch<K, L, 2, GU>(p, st);
-    case 3: return mv1_launch<K, L, 3, GU>(p, st);
-    default: return mv1_launch<K, L, 4, GU>(p, st);
+    case 1: return mv1_launch<K, L, 1, GU, BW>(p, st);
+    case 2: return mv1_launch<K, L, 2, GU, BW>(p, st);
+    case 3: return mv1_launch<K, L, 3, GU, BW>(p, st);
+    default: return mv1_launch<K, L, 4, GU, BW>(p, st);
   }
 }
 
-template <bool GU>
+template <bool GU, bool BW = false>
 static cudaError_t mv1_dispatch(const Mv1Params& p, int k, int L, int M, cudaStream_t st) {
   if (L == 16) {
-    if (k == 2) return mv1_launch_m<2, 16, GU>(p, M, st);
-    if (k == 3) return mv1_launch_m<3, 16, GU>(p, M, st);
-    return mv1_launch_m<4, 16, GU>(p, M, st);
+    if (k == 2) return mv1_launch_m<2, 16, GU, BW>(p, M, st);
+    if (k == 3) return mv1_launch_m<3, 16, GU, BW>(p, M, st);
+    return mv1_launch_m<4, 16, GU, BW>(p, M, st);
   }
-  if (k == 2) return mv1_launch_m<2, 12, GU>(p, M, st);
-  if (k == 3) return mv1_launch_m<3, 12, GU>(p, M, st);
-  return mv1_launch_m<4, 12, GU>(p, M, st);
+  if (k == 2) return mv1_launch_m<2, 12, GU, BW>(p, M, st);
+  if (k == 3) return mv1_launch_m<3, 12, GU, BW>(p, M, st);
+  return mv1_launch_m<4, 12, GU, BW>(p, M, st);
 }
 
 cudaError_t launch_matvec_axis1(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
@@ -242,6 +255,16 @@ cudaError_t launch_matvec_axis1(const uint32_t* codes, const uint16_t* scales, c
   p.scales[0] = p.scales[1] = scales;
   p.x = x; p.out = out; p.R = rows; p.C = cols; p.nb = (int)(cols / kT);
   return mv1_dispatch<false>(p, k, L, M, st);
+}
+
+cudaError_t launch_matvec_axis1_bf16w(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
+                                      uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols,
+                                      cudaStream_t st) {
+  Mv1Params p{};
+  p.codes[0] = p.codes[1] = codes;
+  p.scales[0] = p.scales[1] = scales;
+  p.x = x; p.out = out; p.R = rows; p.C = cols; p.nb = (int)(cols / kT);
+  return mv1_dispatch<false, true>(p, k, L, M, st);
 }
 
 cudaError_t launch_gateup_swiglu(const uint32_t* gcodes, const uint16_t* gscales, const uint32_t* ucodes,
