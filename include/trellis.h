@@ -227,7 +227,10 @@ int trellis_mlp_decode(const uint32_t *gcodes, const uint16_t *gscales, const ui
  *   out[m][r] = bf16( sum_c e(r,c) * x[m][c] ),  e = the bf16 expand weight,
  * accumulated in fp32.
  *   codes [rows][cols*k/32]   scales [rows]   x [M][cols] bf16   out [M][rows] bf16
- * Requires g->axis == 1, M >= 1, and cols a multiple of 64.
+ * Axis 0 (stored W^T, the down projection): out[m][c] = bf16( sum_r e(r,c) *
+ * x[m][r] ), x [M][rows], out [M][cols]; the decoded tile is built from the
+ * stage's code rows staged by TMA, one output feature per decoder thread.
+ * Requires M >= 1, no interleaved layout, and for axis 0 rows % 8 == 0.
  */
 int trellis_gemm_prefill(const uint32_t *codes, const uint16_t *scales, const uint16_t *x,
                          uint16_t *out, int M, const trellis_geom_t *g, trellis_stream_t stream);

@@ -78,7 +78,8 @@ def test_errors_before_launch(lib):
     assert lib.trellis_expand_bf16(A, A, A + 8, ctypes.byref(g), None) == -3
     assert lib.trellis_expand_bf16(A, A, A, ctypes.byref(G(k=7)), None) == -1
     assert lib.trellis_gemm_prefill(A, A, A, A, 0, ctypes.byref(g), None) == -2
-    assert lib.trellis_gemm_prefill(A, A, A, A, 64, ctypes.byref(G(axis=0)), None) == -4
+    assert lib.trellis_gemm_prefill(A, A, A, A, 64, ctypes.byref(G(axis=0, rows=60)), None) == -1  # rows % 8
+    assert lib.trellis_gemm_prefill(A, A, A, A, 64, ctypes.byref(G(k=3, axis=0, cols=1024, interleave=2)), None) == -1
     g0 = G(axis=0)
     need = lib.trellis_workspace_bytes(4, ctypes.byref(g0))
     assert need > 0 and lib.trellis_workspace_bytes(5, ctypes.byref(g0)) == 0

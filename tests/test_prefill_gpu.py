@@ -63,3 +63,25 @@ def test_prefill_L12(oracle_mod):
     out = tb.gemm_prefill(to_dev_u32(codes), to_dev_f16(scales), to_dev_bf16(x), g)
     ref, ab = oracle_mod.prefill(codes, scales, x, 4, 12, T)
     check_band(oracle_mod, bf16_bits(out), ref, ab, "prefill L=12")
+
+
+@pytest.mark.parametrize("k", [2, 3, 4])
+@pytest.mark.parametrize("M,rows,cols", [(5, 256, 256), (40, 1000, 512), (300, 520, 768), (33, 8, 256)])
+def test_prefill_axis0_small(oracle_mod, k, M, rows, cols):
+    """Axis 0 (stored W^T): out[m][c] = sum_r e(r,c) x[m][r] over bf16 expand weights."""
+    codes, scales, x = inputs.make_linear(rows, cols, k, M, seed_codes=121 + k, seed_x=122, sigma=0.5, x_len=rows)
+    g = tb.Geometry(k, L, T, 0, rows, cols)
+    out = tb.gemm_prefill(to_dev_u32(codes), to_dev_f16(scales), to_dev_bf16(x), g)
+    ref, ab = oracle_mod.matvec_axis0_bf16w(codes, scales, x, k, L, T)
+    check_band(oracle_mod, bf16_bits(out), ref, ab, f"prefill axis0 k={k} M={M} {rows}x{cols}")
+
+
+@pytest.mark.parametrize("M", [64, 512])
+def test_prefill_axis0_full_size_sampled(oracle_mod, M):
+    rows, cols, k = 17408, 5120, 3
+    codes, scales, x = inputs.make_linear(rows, cols, k, M, sigma=0.5, x_len=rows)
+    g = tb.Geometry(k, L, T, 0, rows, cols)
+    out = bf16_bits(tb.gemm_prefill(to_dev_u32(codes), to_dev_f16(scales), to_dev_bf16(x), g))
+    idx = np.unique(np.r_[np.arange(0, cols, 331), 127, 128, 255, 256, cols - 1]).astype(np.int64)
+    ref, ab = oracle_mod.matvec_axis0_bf16w(codes, scales, x, k, L, T, cols=idx)
+    check_band(oracle_mod, out[:, idx], ref, ab, f"prefill axis0 full M={M}")

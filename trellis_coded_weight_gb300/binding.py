@@ -209,14 +209,16 @@ def gateup_swiglu(gcodes, gscales, ucodes, uscales, x, g: Geometry, out=None):
 
 
 def gemm_prefill(codes, scales, x, g: Geometry, out=None):
-    """out[M, rows] = x[M, cols] @ E^T with E the bf16 expand weights (tensor cores)."""
+    """Prefill GEMM on the tensor cores with the bf16 expand weights E (stored [rows, cols]):
+    axis 1: out[M, rows] = x[M, cols] @ E^T;  axis 0: out[M, cols] = x[M, rows] @ E."""
     M = x.shape[0]
+    n_in, n_out = (g.cols, g.rows) if g.axis == 1 else (g.rows, g.cols)
     if out is None:
-        out = torch.empty((M, g.rows), dtype=torch.bfloat16, device=x.device)
+        out = torch.empty((M, n_out), dtype=torch.bfloat16, device=x.device)
     args = (_req(codes, "codes", _CODES, g.codes_shape),
             _req(scales, "scales", (torch.float16,), (g.rows,)),
-            _req(x, "x", (torch.bfloat16,), (M, g.cols)),
-            _req(out, "out", (torch.bfloat16,), (M, g.rows)))
+            _req(x, "x", (torch.bfloat16,), (M, n_in)),
+            _req(out, "out", (torch.bfloat16,), (M, n_out)))
     _check("trellis_gemm_prefill", load().trellis_gemm_prefill(*args, M, ctypes.byref(g.c()), _stream(x)))
     return out
 

@@ -207,12 +207,13 @@ int trellis_gemm_prefill(const uint32_t* codes, const uint16_t* scales, const ui
                          const trellis_geom_t* g, trellis_stream_t stream) {
   int st = geom_ok(g);
   if (st) return st;
-  if (g->axis != 1) return TRELLIS_EAXIS;
+  if (g->interleave) return TRELLIS_EGEOM;
+  if (g->axis == 0 && g->rows % 8 != 0) return TRELLIS_EGEOM;  // x rows of axis 0 must be 16-byte multiples
   if (M < 1 || M > (1 << 24)) return TRELLIS_EM;
   if (!codes || !scales || !x || !out) return TRELLIS_ENULL;
   if (!aligned16(codes) || !aligned16(scales) || !aligned16(x) || !aligned16(out)) return TRELLIS_EALIGN;
   if ((st = device_ok())) return st;
-  return cuda_status(trellis::launch_gemm_prefill(codes, scales, x, out, M, g->k, g->L, g->rows, g->cols,
+  return cuda_status(trellis::launch_gemm_prefill(codes, scales, x, out, M, g->k, g->L, g->axis, g->rows, g->cols,
                                                   static_cast<cudaStream_t>(stream)));
 }
 

@@ -38,7 +38,7 @@ cudaError_t launch_matvec_axis0(const uint32_t* codes, const uint16_t* scales, c
                                 void* workspace, cudaStream_t st);
 
 cudaError_t launch_gemm_prefill(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
-                                uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols,
+                                uint16_t* out, int M, int k, int L, int axis, int64_t rows, int64_t cols,
                                 cudaStream_t st);
 
 // Device error word of the tensor-core kernels (bounded waits that gave up).

@@ -59,22 +59,27 @@ struct PrefillParams {
   const uint32_t* codes;
   const uint16_t* scales;
   uint16_t* out;
-  int64_t R, C;
+  int64_t R, C;     // stored rows and coded columns
+  int64_t nOut;     // output features: R for axis 1, C for axis 0
+  int64_t Kd;       // reduction length: C for axis 1, R for axis 0
   int M, nb;
-  int nRT, nTiles;  // row tiles, total tiles
-  int tma_out;      // 1: out written by TMA tensor stores (R % 8 == 0)
+  int nRT, nTiles;  // output-feature tiles, total tiles
+  int tma_out;      // 1: out written by TMA tensor stores (nOut % 8 == 0)
 };
 
-template <int BN, int BK>
+// CT: bytes of the per-stage code tile (axis 0 only; 0 for axis 1).
+template <int BN, int BK, int CT = 0>
 struct Cfg {
   static constexpr int NACC = 2 * BN <= 512 ? 2 : 1;  // accumulators in tensor memory
   static constexpr int NMMA = BN > 256 ? 256 : BN;    // MMA N
   static constexpr int NH = BN / NMMA;                 // MMAs along N per 16 columns
   static constexpr int ATile = kBM * BK * 2;
   static constexpr int BTile = BN * BK * 2;
-  static constexpr int Stage = ATile + BTile;
+  static constexpr int CTile = CT;
+  static constexpr int Stage = ATile + BTile + CTile;
   static constexpr int EpiBytes = kEpiWarps * 2 * 32 * 32 * 2;  // per warp: two 32x32 bf16 sub-tiles
-  static constexpr int NS0 = (220 * 1024 - EpiBytes) / Stage;
+  static constexpr int ScaleBytes = CT ? kDecWarps * 32 * 4 : 0;  // per-warp row scales (axis 0)
+  static constexpr int NS0 = (220 * 1024 - EpiBytes - ScaleBytes) / Stage;
   static constexpr int NS = NS0 > 8 ? 8 : NS0;         // ring stages
   static constexpr int TmemCols = NACC * BN < 32 ? 32 : NACC * BN;
   static constexpr int RunsPerRow = BK / 32;            // runs of 32 positions per row and stage
@@ -83,7 +88,7 @@ struct Cfg {
   static constexpr uint32_t SBO = 8u * BK * 2u;         // bytes between 8-row groups
   static constexpr uint32_t SwMode = BK == 64 ? 2u : 4u;  // descriptor swizzle: 128B or 64B
   static constexpr CUtensorMapSwizzle TmaSw = BK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-  static constexpr size_t Smem = 1024 + (size_t)NS * Stage + EpiBytes + 512;
+  static constexpr size_t Smem = 1024 + (size_t)NS * Stage + EpiBytes + ScaleBytes + 512;
   static_assert(BK == 64 || BK == 32, "stage width");
   static_assert(NS >= 2, "ring too small");
 };
@@ -130,13 +135,42 @@ __device__ __forceinline__ void decode_run_to_tile(const RunWords<K>& rw, uint8_
         make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
 }
 
+// Axis 0: decode, for one output feature (a fixed position of a block, so a
+// fixed window offset), the weights of 32 consecutive stored rows from the
+// stage's code tile ct [rows][WPB words], scale each by its row's scale, and
+// write them as bf16 into the A row of that feature (K-major, swizzled).
+template <int K, int L>
+__device__ __forceinline__ void decode_col_to_tile(const uint32_t* ct, int row0, int t, const float* sc,
+                                                   uint8_t* row, int sw, int chunk0) {
+  constexpr int WPB = kT * K / 32;
+  const int o = (kT - 1 - t) * K, wi = o >> 5, sh = o & 31;
+  const int wj = (wi + 1 == WPB) ? 0 : wi + 1;
+  const uint32_t mask = (L == 32) ? 0xFFFFFFFFu : ((1u << L) - 1u);
+  const float2 nmagic = make_float2(-kMagic, -kMagic);
+  uint32_t packed[16];
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    const uint32_t* w0 = ct + (row0 + j) * WPB;
+    const uint32_t* w1 = w0 + WPB;
+    const uint32_t s0 = __funnelshift_r(w0[wi], w0[wj], sh) & mask;
+    const uint32_t s1 = __funnelshift_r(w1[wi], w1[wj], sh) & mask;
+    const float2 y = __fadd2_rn(make_float2(__uint_as_float(code_magic(s0)), __uint_as_float(code_magic(s1))), nmagic);
+    const float2 wv = __fmul2_rn(value_rn2(y), make_float2(sc[j], sc[j + 1]));
+    packed[j / 2] = pack_bf16x2(wv.x, wv.y);
+  }
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    *reinterpret_cast<uint4*>(row + (((chunk0 + c) ^ sw) << 4)) =
+        make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+}
+
 __device__ __forceinline__ void report(int code) { atomicCAS(&g_device_error, 0, code); }
 
-template <int K, int L, int BN, int BK>
+template <int K, int L, int BN, int BK, int AX>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_out,
-                   const PrefillParams p) {
-  using C_ = Cfg<BN, BK>;
+                   const __grid_constant__ CUtensorMap tmap_codes, const PrefillParams p) {
+  using C_ = Cfg<BN, BK, AX == 0 ? BK * (kT * K / 32) * 4 : 0>;
   constexpr int NS = C_::NS, NACC = C_::NACC, NMMA = C_::NMMA, NH = C_::NH;
   constexpr int WPB = kT * K / 32;
   constexpr int RowBytes = BK * 2;
@@ -146,8 +180,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* a_tiles = smem;                                // NS x ATile
   uint8_t* b_tiles = smem + (size_t)NS * C_::ATile;       // NS x BTile
+  uint8_t* c_tiles = b_tiles + (size_t)NS * C_::BTile;   // NS x CTile (axis 0: code words of the stage)
   uint8_t* epi_stage = smem + (size_t)NS * C_::Stage;     // kEpiWarps x 2 x [32 tokens][32 rows] bf16
-  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_stage + C_::EpiBytes);
+  float* sbuf = reinterpret_cast<float*>(epi_stage + C_::EpiBytes);  // axis 0: 32 row scales per decoder warp
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_stage + C_::EpiBytes + C_::ScaleBytes);
   uint64_t* full_a = bars;                 // decoder group -> MMA
   uint64_t* full_b = bars + NS;            // TMA -> MMA (1 arrival + tx bytes)
   uint64_t* empty = bars + 2 * NS;         // MMA commit -> producer and decoders
@@ -159,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x;
   const int n_local = (p.nTiles - (int)blockIdx.x + G - 1) / G;
-  const int nk = (int)(p.C / BK);
+  const int nk = (int)((p.Kd + BK - 1) / BK);  // the last stage may run past Kd: TMA fills zeros
   const int64_t total = (int64_t)n_local * nk;  // stages this CTA runs
 
   if (threadIdx.x == 0) {
@@ -194,7 +230,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ks = 0; ks < nk; ++ks, ++g) {
           const int s = (int)(g % NS);
           if (g >= NS && !tc::mbar_wait(empty + s, (uint32_t)((g / NS) & 1) ^ 1u, kWaitNs)) { *fail = 1; break; }
-          tc::mbar_arrive_expect_tx(full_b + s, (uint32_t)C_::BTile);
+          tc::mbar_arrive_expect_tx(full_b + s, (uint32_t)(C_::BTile + C_::CTile));
+          if constexpr (AX == 0)  // the codes of this stage's stored rows, for the tile's block
+            tc::tma_load_2d(c_tiles + (size_t)s * C_::CTile, &tmap_codes, full_b + s, ((t % p.nRT) >> 1) * WPB,
+                            ks * BK);
 #pragma unroll
           for (int h = 0; h < NH; ++h)
             tc::tma_load_2d(b_tiles + (size_t)s * C_::BTile + (size_t)h * NMMA * RowBytes, &tmap_x, full_b + s,
@@ -268,18 +307,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc::fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0 && m0 + c0 < p.M && rbase < p.R) {
+          if (lane == 0 && m0 + c0 < p.M && rbase < p.nOut) {
             tc::tma_store_2d(&tmap_out, st, (int)rbase, m0 + c0);
             tc::bulk_commit();
           }
-        } else if (row < p.R) {
+        } else if (row < p.nOut) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int m = m0 + c0 + i;
             if (m < p.M) {
               uint16_t o;
               asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(o) : "f"(__uint_as_float(v[i])));
-              p.out[(int64_t)m * p.R + row] = o;
+              p.out[(int64_t)m * p.nOut + row] = o;
             }
           }
         }
@@ -299,36 +338,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rl = (gw & 3) * 32 + lane;   // tile row of this thread
     const int h = gw >> 2;                 // which run of the stage
     const int sw = BK == 64 ? (rl & 7) : ((rl >> 1) & 3);
-    auto fetch = [&](RunWords<K>& rw, int64_t g) {
-      if (g >= total) return;
-      const int lt = (int)(g / nk), ks = (int)(g % nk);
-      const int t = (int)blockIdx.x + lt * G;
-      int64_t r = (int64_t)(t % p.nRT) * kBM + rl;
-      if (r >= p.R) r = p.R - 1;  // rows past the end decode row R-1 and are never stored
-      const int c = ks * BK + 32 * h;  // first column of the run
-      load_run<K>(rw, p.codes + (r * p.nb + c / kT) * WPB, (c % kT) / 32, p.scales + r);
-    };
-    auto process = [&](const RunWords<K>& rw, int64_t g) -> bool {
-      const int s = (int)(g % NS);
-      if (g >= NS && !tc::mbar_wait(empty + s, (uint32_t)((g / NS) & 1) ^ 1u, kWaitNs)) return false;
-      decode_run_to_tile<K, L>(rw, a_tiles + (size_t)s * C_::ATile + rl * RowBytes, sw, 4 * h);
-      tc::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(full_a + s);
-      return true;
-    };
-    RunWords<K> ra, rb;
-    int64_t g = grp;
-    fetch(ra, g);
-    fetch(rb, g + NG);
-    while (g < total) {
-      if (!process(ra, g)) { *fail = 1; break; }
-      fetch(ra, g + 2 * NG);
-      g += NG;
-      if (g >= total) break;
-      if (!process(rb, g)) { *fail = 1; break; }
-      fetch(rb, g + 2 * NG);
-      g += NG;
+    if constexpr (AX == 0) {
+      // one output feature per thread (fixed window offset), 32 stored rows per run
+      float* sb = sbuf + dw * 32;
+      auto scale_of = [&](int64_t g) -> float {
+        if (g >= total) return 0.f;
+        int64_t r = (int64_t)(g % nk) * BK + 32 * h + lane;
+        if (r >= p.R) r = p.R - 1;
+        return f16_to_f32(__ldg(p.scales + r));
+      };
+      float nsc = scale_of(grp);
+      for (int64_t g = grp; g < total; g += NG) {
+        const int s = (int)(g % NS);
+        const uint32_t ph = (uint32_t)((g / NS) & 1);
+        __syncwarp();
+        sb[lane] = nsc;
+        nsc = scale_of(g + NG);
+        __syncwarp();
+        if (g >= NS && !tc::mbar_wait(empty + s, ph ^ 1u, kWaitNs)) { *fail = 1; break; }
+        if (!tc::mbar_wait(full_b + s, ph, kWaitNs)) { *fail = 1; break; }  // the code tile has landed
+        const int t = (int)blockIdx.x + (int)(g / nk) * G;
+        const int tpos = (((t % p.nRT) * kBM) & (kT - 1)) + rl;  // position of this feature in its block
+        decode_col_to_tile<K, L>(reinterpret_cast<const uint32_t*>(c_tiles + (size_t)s * C_::CTile), 32 * h, tpos,
+                                 sb, a_tiles + (size_t)s * C_::ATile + rl * RowBytes, sw, 4 * h);
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(full_a + s);
+      }
+    } else {
+      auto fetch = [&](RunWords<K>& rw, int64_t g) {
+        if (g >= total) return;
+        const int lt = (int)(g / nk), ks = (int)(g % nk);
+        const int t = (int)blockIdx.x + lt * G;
+        int64_t r = (int64_t)(t % p.nRT) * kBM + rl;
+        if (r >= p.R) r = p.R - 1;  // rows past the end decode row R-1 and are never stored
+        const int c = ks * BK + 32 * h;  // first column of the run
+        load_run<K>(rw, p.codes + (r * p.nb + c / kT) * WPB, (c % kT) / 32, p.scales + r);
+      };
+      auto process = [&](const RunWords<K>& rw, int64_t g) -> bool {
+        const int s = (int)(g % NS);
+        if (g >= NS && !tc::mbar_wait(empty + s, (uint32_t)((g / NS) & 1) ^ 1u, kWaitNs)) return false;
+        decode_run_to_tile<K, L>(rw, a_tiles + (size_t)s * C_::ATile + rl * RowBytes, sw, 4 * h);
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(full_a + s);
+        return true;
+      };
+      RunWords<K> ra, rb;
+      int64_t g = grp;
+      fetch(ra, g);
+      fetch(rb, g + NG);
+      while (g < total) {
+        if (!process(ra, g)) { *fail = 1; break; }
+        fetch(ra, g + 2 * NG);
+        g += NG;
+        if (g >= total) break;
+        if (!process(rb, g)) { *fail = 1; break; }
+        fetch(rb, g + 2 * NG);
+        g += NG;
+      }
     }
   }
 
@@ -361,15 +429,18 @@ int sm_count() {
   return n;
 }
 
-template <int K, int L, int BN, int BK>
+template <int K, int L, int BN, int BK, int AX>
 cudaError_t prefill_launch(PrefillParams p, const uint16_t* x, cudaStream_t st) {
-  using C_ = Cfg<BN, BK>;
+  constexpr int WPB = kT * K / 32;
+  using C_ = Cfg<BN, BK, AX == 0 ? BK * WPB * 4 : 0>;
   auto fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
-  CUtensorMap map, omap;
-  {
-    const cuuint64_t dims[2] = {(cuuint64_t)p.C, (cuuint64_t)p.M};
-    const cuuint64_t strides[1] = {(cuuint64_t)p.C * 2};
+  CUtensorMap map, omap, cmap;
+  memset(&omap, 0, sizeof(omap));
+  memset(&cmap, 0, sizeof(cmap));
+  {  // x [M][Kd] bf16, boxes of [NMMA tokens][BK columns], swizzled
+    const cuuint64_t dims[2] = {(cuuint64_t)p.Kd, (cuuint64_t)p.M};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.Kd * 2};
     const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)C_::NMMA};
     const cuuint32_t estr[2] = {1, 1};
     if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, estr,
@@ -377,11 +448,20 @@ cudaError_t prefill_launch(PrefillParams p, const uint16_t* x, cudaStream_t st) 
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  memset(&omap, 0, sizeof(omap));
+  if (AX == 0) {  // codes [R][C*k/32] uint32, boxes of [BK stored rows][one block of words]
+    const cuuint64_t dims[2] = {(cuuint64_t)(p.C * K / 32), (cuuint64_t)p.R};
+    const cuuint64_t strides[1] = {(cuuint64_t)(p.C * K / 32) * 4};
+    const cuuint32_t box[2] = {(cuuint32_t)WPB, (cuuint32_t)BK};
+    const cuuint32_t estr[2] = {1, 1};
+    if (fn(&cmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(p.codes), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   p.tma_out = 0;
-  if (p.R % 8 == 0) {  // out rows are 16-byte multiples: tensor stores of [32 tokens][32 rows] boxes
-    const cuuint64_t dims[2] = {(cuuint64_t)p.R, (cuuint64_t)p.M};
-    const cuuint64_t strides[1] = {(cuuint64_t)p.R * 2};
+  if (p.nOut % 8 == 0) {  // out rows are 16-byte multiples: tensor stores of [32 tokens][32 features] boxes
+    const cuuint64_t dims[2] = {(cuuint64_t)p.nOut, (cuuint64_t)p.M};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.nOut * 2};
     const cuuint32_t box[2] = {32, 32};
     const cuuint32_t estr[2] = {1, 1};
     if (fn(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.out, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -389,45 +469,52 @@ cudaError_t prefill_launch(PrefillParams p, const uint16_t* x, cudaStream_t st) 
         CUDA_SUCCESS)
       p.tma_out = 1;
   }
-  auto kern = prefill_kernel<K, L, BN, BK>;
+  auto kern = prefill_kernel<K, L, BN, BK, AX>;
   static bool attr_set = false;  // per instantiation
   if (!attr_set) {
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_::Smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  p.nRT = (int)((p.R + kBM - 1) / kBM);
+  p.nRT = (int)((p.nOut + kBM - 1) / kBM);
   p.nTiles = p.nRT * ((p.M + BN - 1) / BN);
   const int sms = sm_count();
   const int grid = p.nTiles < sms ? p.nTiles : sms;
-  kern<<<grid, kThreads, C_::Smem, st>>>(map, omap, p);
+  kern<<<grid, kThreads, C_::Smem, st>>>(map, omap, cmap, p);
   return cudaGetLastError();
 }
 
-template <int K, int L>
+template <int K, int L, int AX>
 cudaError_t prefill_bn(const PrefillParams& p, const uint16_t* x, cudaStream_t st) {
-  if (p.M <= 32) return prefill_launch<K, L, 32, 64>(p, x, st);
-  if (p.M <= 64) return prefill_launch<K, L, 64, 64>(p, x, st);
-  if (p.M <= 128) return prefill_launch<K, L, 128, 64>(p, x, st);
-  if (p.M <= 256) return prefill_launch<K, L, 256, 64>(p, x, st);
-  return prefill_launch<K, L, 512, 32>(p, x, st);
+  if (p.M <= 32) return prefill_launch<K, L, 32, 64, AX>(p, x, st);
+  if (p.M <= 64) return prefill_launch<K, L, 64, 64, AX>(p, x, st);
+  if (p.M <= 128) return prefill_launch<K, L, 128, 64, AX>(p, x, st);
+  if (p.M <= 256) return prefill_launch<K, L, 256, 64, AX>(p, x, st);
+  return prefill_launch<K, L, 512, 32, AX>(p, x, st);
+}
+
+template <int AX>
+cudaError_t prefill_axis(const PrefillParams& p, const uint16_t* x, int k, int L, cudaStream_t st) {
+  if (L == 16) {
+    if (k == 2) return prefill_bn<2, 16, AX>(p, x, st);
+    if (k == 3) return prefill_bn<3, 16, AX>(p, x, st);
+    return prefill_bn<4, 16, AX>(p, x, st);
+  }
+  if (k == 2) return prefill_bn<2, 12, AX>(p, x, st);
+  if (k == 3) return prefill_bn<3, 12, AX>(p, x, st);
+  return prefill_bn<4, 12, AX>(p, x, st);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_prefill(const uint32_t* codes, const uint16_t* scales, const uint16_t* x, uint16_t* out,
-                                int M, int k, int L, int64_t rows, int64_t cols, cudaStream_t st) {
+                                int M, int k, int L, int axis, int64_t rows, int64_t cols, cudaStream_t st) {
   PrefillParams p{};
   p.codes = codes; p.scales = scales; p.out = out;
   p.R = rows; p.C = cols; p.M = M; p.nb = (int)(cols / kT);
-  if (L == 16) {
-    if (k == 2) return prefill_bn<2, 16>(p, x, st);
-    if (k == 3) return prefill_bn<3, 16>(p, x, st);
-    return prefill_bn<4, 16>(p, x, st);
-  }
-  if (k == 2) return prefill_bn<2, 12>(p, x, st);
-  if (k == 3) return prefill_bn<3, 12>(p, x, st);
-  return prefill_bn<4, 12>(p, x, st);
+  p.nOut = axis == 1 ? rows : cols;
+  p.Kd = axis == 1 ? cols : rows;
+  return axis == 1 ? prefill_axis<1>(p, x, k, L, st) : prefill_axis<0>(p, x, k, L, st);
 }
 
 // Read (and optionally clear) the device error word.
