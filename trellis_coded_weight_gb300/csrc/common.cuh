@@ -88,17 +88,18 @@ __device__ __forceinline__ uint32_t window_at(const uint32_t (&w)[NW], int O) {
   return (off + L == 32) ? v : (v & ((1u << L) - 1u));
 }
 
-// States of the 32 positions t0 .. t0+31 of a run.  Position t0+j starts at
-// run bit (31-j)*K; w[0..K] are the run's K words followed by the spill word.
-// For L = 16 and K in {2, 4}, windows 16 bits apart come from one 32-bit
-// funnel shift: the low half is one state and the high half the other.
-template <int K, int L>
-__device__ __forceinline__ void run_states(const uint32_t (&w)[K + 1], uint32_t (&s)[32]) {
+// States of the N positions t0 .. t0+N-1 of a run.  Position t0+j starts at
+// run bit (N-1-j)*K; w[] holds the run's words, aligned so that w[0] bit 0 is
+// run bit 0, followed by the spill word.  For L = 16 and K in {2, 4}, windows
+// 16 bits apart come from one 32-bit funnel shift: the low half is one state
+// and the high half the other.
+template <int K, int L, int N = 32, int NW = K + 1>
+__device__ __forceinline__ void run_states(const uint32_t (&w)[NW], uint32_t (&s)[N]) {
   constexpr bool kPair = (L == 16) && (K == 2 || K == 4);
   constexpr int kPartner = 16 / K;  // j - kPartner starts 16 bits above j
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const int o = (31 - j) * K;
+  for (int j = 0; j < N; ++j) {
+    const int o = (N - 1 - j) * K;
     if (kPair) {
       if ((o & 31) < 16) {
         const uint32_t F = (o & 31) ? __funnelshift_r(w[o >> 5], w[(o >> 5) + 1], o & 31) : w[o >> 5];
@@ -106,7 +107,7 @@ __device__ __forceinline__ void run_states(const uint32_t (&w)[K + 1], uint32_t 
         s[j - kPartner] = F >> 16;
       }
     } else {
-      s[j] = window_at<L, K + 1>(w, o);
+      s[j] = window_at<L, NW>(w, o);
     }
   }
 }
