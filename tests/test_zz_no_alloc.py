@@ -62,7 +62,7 @@ def test_noalloc_matches_workspace_call_twice(oracle_mod, lib, first, second):
 
 
 def test_noalloc_rejects_problems_beyond_the_scratch(lib):
-    g = tb.Geometry(2, L, T, 0, 131072, 65536)
+    g = tb.Geometry(2, L, T, 0, 131072, 262144)
     assert tb.workspace_bytes(4, g) > SCRATCH_MAX
     dummy = torch.empty(16, dtype=torch.int32, device="cuda")
     p = dummy.data_ptr()

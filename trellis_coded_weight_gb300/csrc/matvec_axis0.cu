@@ -7,28 +7,30 @@
 // The pages split the sum over stored rows into 128 slices, write every
 // slice's partial vector and fold them with a separate reduction.
 //
-// GB300 design:
-//   * a CTA owns one column block (256 outputs) and one contiguous slice of
-//     the stored rows; the number of slices is chosen so that all CTAs are
-//     resident at once (about five per SM on 152 SMs).
+// GB300 design (a balanced, persistent split over the stored rows):
+//   * the work is the list of (column block, stored row) pairs, column block
+//     major; CTA c of G (one per SM) takes the contiguous range
+//     [c*N/G, (c+1)*N/G) of it, so every SM decodes the same number of rows.
+//     A range crosses at most a few column blocks; each piece is a segment.
 //   * a warp takes two stored rows at a time, one per half-warp; lane j of a
 //     half owns outputs 16j .. 16j+15 of the column block: per row it loads
 //     the two or three words that cover its 16 windows (already word-aligned
 //     for even k) and takes the windows with compile-time shifts, two 16-bit
 //     windows per funnel shift when L = 16 and k is even.  The CTA's warps
-//     take interleaved row pairs.
-//   * x[m][r]*scale[r] is staged once per CTA in shared memory and read with
-//     a broadcast load per row; 1/d is applied after the sum.  The first code
-//     words are requested before the staging so that their latency overlaps it.
-//   * the CTA folds its warps in shared memory.  The slices of a column block
-//     go in thread-block clusters of kAx0Cluster CTAs: each CTA of a cluster
-//     folds its share of the outputs over the cluster's CTAs through
-//     distributed shared memory and writes one fp32 partial per output to the
-//     workspace.  The last CTA to arrive for a column block (an atomic
-//     counter) folds the S / kAx0Cluster cluster partials in order, stores
-//     bf16 and resets the counter -- one launch, deterministic, no atomics on
-//     data.
+//     take interleaved row pairs; the code words of the next group of rows
+//     load while the current group decodes.
+//   * x[m][r]*scale[r] of the segment's rows is staged in shared memory (in
+//     pieces of at most kAx0StageRows rows) and read with a broadcast load per
+//     row; 1/d is applied after the sum.
+//   * at the end of a segment the CTA folds its warps in shared memory and
+//     writes one fp32 partial per output to the workspace, in slot c + cb
+//     (unique per CTA and column block).  Arrivals are published at the end
+//     of the range (one fence for all its segments).  The last CTA to arrive
+//     for a column block (an atomic counter against the known number of CTAs
+//     that cover it) folds the partials in CTA order, stores bf16 and resets
+//     the counter -- one launch, deterministic, no atomics on data.
 #include <cstdint>
+#include <mutex>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -36,53 +38,21 @@
 
 namespace trellis {
 
-constexpr int kAx0Warps = 4;
-constexpr int kAx0Chunk = 4;    // row pairs per prefetch chunk
-constexpr int kAx0Cluster = 8;  // CTAs (row slices) per thread-block cluster
-constexpr int64_t kAx0TargetCtas = 152 * 5;
+constexpr int kAx0Chunk = 4;             // rows per lane per prefetch group
+constexpr int kAx0MaxCtas = 256;         // bound on the grid (sizes the workspace)
+constexpr int64_t kAx0MinRows = 64;      // fewest (column block, row) pairs per CTA
+constexpr int64_t kAx0StageRows = 2048;  // rows of x*scale staged at once
+constexpr int kAx0MaxPending = 4;        // segments whose arrival waits for one fence
 
-struct Ax0Plan {
-  int nb;       // column blocks
-  int S;        // row slices, a multiple of kAx0Cluster
-  int64_t rps;  // rows per slice
-};
-
-static Ax0Plan ax0_plan(int64_t rows, int64_t cols) {
-  Ax0Plan p;
-  p.nb = (int)(cols / kT);
-  int64_t rps = (rows * p.nb + kAx0TargetCtas - 1) / kAx0TargetCtas;
-  if (rps < 32) rps = 32;
-  if (rps > 1600) rps = 1600;  // keeps the staged slice (and its scales) within 48 KB of shared memory
-  int64_t S = (rows + rps - 1) / rps;
-  S = (S + kAx0Cluster - 1) / kAx0Cluster * kAx0Cluster;
-  p.S = (int)S;
-  p.rps = (rows + S - 1) / S;  // trailing slices may be short or empty
-  return p;
-}
+// Warps per CTA: as many as the accumulators' registers allow with one CTA per SM.
+template <int M>
+__host__ __device__ constexpr int ax0_warps() { return M <= 2 ? 16 : 12; }
 
 size_t axis0_workspace_bytes(int M, int64_t rows, int64_t cols) {
-  const Ax0Plan p = ax0_plan(rows, cols);
-  const size_t part = (size_t)(p.S / kAx0Cluster) * (size_t)M * (size_t)cols * sizeof(float);
-  return part + (((size_t)p.nb * sizeof(uint32_t) + 15) & ~(size_t)15);
-}
-
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// fp32 at the same shared-memory offset in CTA `rank` of this cluster.
-__device__ __forceinline__ float ld_dsmem(const float* local, uint32_t rank) {
-  uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local)), r;
-  float v;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(r) : "memory");
-  return v;
+  (void)rows;
+  const int64_t nb = cols / kT;
+  const size_t part = (size_t)(kAx0MaxCtas + nb) * (size_t)M * kT * sizeof(float);
+  return part + (((size_t)nb * sizeof(uint32_t) + 15) & ~(size_t)15);
 }
 
 struct Ax0Params {
@@ -90,272 +60,329 @@ struct Ax0Params {
   const uint16_t* scales;
   const uint16_t* x;
   uint16_t* out;
-  float* part;        // [S / kAx0Cluster][M][cols]
+  float* part;        // [kAx0MaxCtas + nb][M][256]
   uint32_t* counter;  // [nb]
-  int64_t R, C, rps;
-  int nb, S;
-  int interleave;  // 2: codes in the [nb/2][R][2*WPB] layout
+  int64_t R, C, N;    // rows, cols, N = nb * R work items
+  int nb, G;          // column blocks, CTAs
+  int stage;          // rows staged at once (<= kAx0StageRows)
 };
 
-template <int K, int L, int M, bool BW>
-__global__ void __launch_bounds__(32 * kAx0Warps) ax0_kernel(const Ax0Params p) {
+// The CTA whose range holds work item f: the largest c with c*N/G <= f.
+__device__ __forceinline__ int ax0_cta_of(int64_t f, int64_t N, int G) { return (int)(((f + 1) * G - 1) / N); }
+
+template <int K, int L, int M, bool BW, bool IL>
+__global__ void __launch_bounds__(32 * ax0_warps<M>(), 1) ax0_kernel(const Ax0Params p) {
+  constexpr int W = ax0_warps<M>();
   constexpr int WPB = kT * K / 32;
   // Words of one lane's 16-position run: 15K + L bits, plus up to 16 bits of
   // misalignment when K is odd.
   constexpr bool kEven = (K % 2) == 0;
   constexpr int NR = (15 * K + L + (kEven ? 0 : 16) + 31) / 32;
+  constexpr int G = kAx0Chunk;
+  constexpr int RS = 2 * W;  // rows per CTA step
   extern __shared__ __align__(16) float smem[];
-  float* xs = smem;                        // [rps][M]  x*scale of this slice's rows
-  float* red = smem + ((p.rps * M + 3) & ~(int64_t)3);  // [warps][M][256], 16-byte aligned
-  float* scs = red + kAx0Warps * M * kT;                 // [rps] row scales (bf16-weight numerics)
-  __shared__ uint32_t last_flag;
+  float* xs = smem;                                       // [stage][M]  x*scale of the staged rows
+  float* red = smem + ((p.stage * M + 3) & ~3);           // [W][M][256], 16-byte aligned
+  float* scs = red + W * M * kT;                          // [stage] row scales (bf16-weight numerics)
+  __shared__ int pend[kAx0MaxPending];          // column blocks whose arrival is pending
+  __shared__ uint32_t is_last[kAx0MaxPending];
+  int npend = 0;
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int half = lane >> 4, j = lane & 15;
-  const int cb = blockIdx.x, sl = blockIdx.y;
-  const int64_t r0 = (int64_t)sl * p.rps;
-  const int64_t r1 = (r0 + p.rps < p.R) ? r0 + p.rps : p.R;
-  const int nr = r1 > r0 ? (int)(r1 - r0) : 0;
-
+  const int rb = 2 * warp + half;  // this lane's first row of every staged piece
   // Half-warp `half` takes the odd or even row of each row pair; lane j of
   // the half owns block positions 16j .. 16j+15, whose windows start at
   // block bits (255-16j-i)*K, the lowest at lo = (240-16j)*K.
   const int lo = (kT - 16 * (j + 1)) * K;
   const int wa = lo >> 5, sh = lo & 31;
-  int widx[NR];
-#pragma unroll
-  for (int i = 0; i < NR; ++i) widx[i] = (wa + i >= WPB) ? wa + i - WPB : wa + i;
-  // row stride and first word of column block cb in either layout
-  const int64_t rowWords = p.interleave ? 2 * WPB : (int64_t)p.nb * WPB;
-  const uint32_t* base = p.interleave ? p.codes + (int64_t)(cb >> 1) * p.R * (2 * WPB) + (cb & 1) * WPB
-                                      : p.codes + (int64_t)cb * WPB;
-
-  // This warp's row pairs are warp, warp + W, ... (W warps per CTA); row
-  // pair q holds rows 2q and 2q+1 of the slice.  They go in chunks of
-  // kAx0Chunk pairs; the code words of the next chunk load while the current
-  // chunk decodes.  Rows past the slice load a valid row and are skipped.
-  const int np = (nr + 1) >> 1;
-  const int nw = np > warp ? (np - warp + kAx0Warps - 1) / kAx0Warps : 0;
-  const int nch = (nw + kAx0Chunk - 1) / kAx0Chunk;
-  auto row_of = [&](int i) { return 2 * (warp + i * kAx0Warps) + half; };
-  auto load_chunk = [&](uint32_t (&a)[kAx0Chunk][NR], int ch) {
-#pragma unroll
-    for (int u = 0; u < kAx0Chunk; ++u) {
-      int i = ch * kAx0Chunk + u;
-      if (i >= nw) i = nw - 1;
-      int rl = row_of(i);
-      if (rl >= nr) rl = nr - 1;
-      const uint32_t* rw = base + (r0 + rl) * rowWords;
-#pragma unroll
-      for (int q = 0; q < NR; ++q) a[u][q] = __ldg(rw + widx[q]);
-    }
-  };
-  uint32_t a0[kAx0Chunk][NR], a1[kAx0Chunk][NR];
-  if (nch > 0) load_chunk(a0, 0);
-
-  // stage x*scale (or x and the scales) of the slice, four rows per thread in flight
-  for (int rb = threadIdx.x; rb < nr; rb += 4 * blockDim.x) {
-    float sv[4], xv[4][M];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int rl = rb + u * (int)blockDim.x;
-      const int64_t r = r0 + (rl < nr ? rl : 0);
-      sv[u] = f16_to_f32(__ldg(p.scales + r));
-#pragma unroll
-      for (int m = 0; m < M; ++m) xv[u][m] = bf16_to_f32(__ldg(p.x + (int64_t)m * p.R + r));
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int rl = rb + u * (int)blockDim.x;
-      if (rl < nr) {
-        // default numerics fold the row scale into x; bf16 weights need it per weight
-#pragma unroll
-        for (int m = 0; m < M; ++m) xs[rl * M + m] = BW ? xv[u][m] : __fmul_rn(xv[u][m], sv[u]);
-        if (BW) scs[rl] = sv[u];
-      }
-    }
-  }
-  __syncthreads();
-
+  const int64_t rowWords = IL ? 2 * WPB : (int64_t)p.nb * WPB;
   const float2 nmagic = make_float2(-kMagic, -kMagic);
-  float2 acc[M][8];
-#pragma unroll
-  for (int m = 0; m < M; ++m)
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[m][i] = make_float2(0.f, 0.f);
 
-  auto body = [&](const uint32_t (&raw)[NR], int rl) {
-    uint32_t w[NR];
-    if constexpr (kEven) {
+  const int c = blockIdx.x;
+  const int64_t f1 = (int64_t)(c + 1) * p.N / p.G;
+  for (int64_t f = (int64_t)c * p.N / p.G; f < f1;) {
+    const int cb = (int)(f / p.R);
+    const int64_t sa = f - (int64_t)cb * p.R;
+    const int64_t se = (f1 - (int64_t)cb * p.R < p.R) ? f1 - (int64_t)cb * p.R : p.R;
+    f = (int64_t)cb * p.R + se;
+    // first word of column block cb in either layout
+    const uint32_t* base = IL ? p.codes + (int64_t)(cb >> 1) * p.R * (2 * WPB) + (cb & 1) * WPB
+                              : p.codes + (int64_t)cb * WPB;
+
+    float2 acc[M][8];
 #pragma unroll
-      for (int i = 0; i < NR; ++i) w[i] = raw[i];
-    } else {
+    for (int m = 0; m < M; ++m)
 #pragma unroll
-      for (int i = 0; i + 1 < NR; ++i) w[i] = __funnelshift_r(raw[i], raw[i + 1], sh);
-      w[NR - 1] = raw[NR - 1] >> sh;
-    }
-    uint32_t s[16];
-    run_states<K, L, 16, NR>(w, s);
-    float xr[M];
-    if constexpr (M == 4) {
-      const float4 v = *reinterpret_cast<const float4*>(xs + rl * 4);
-      xr[0] = v.x; xr[1] = v.y; xr[2] = v.z; xr[3] = v.w;
-    } else {
+      for (int i = 0; i < 8; ++i) acc[m][i] = make_float2(0.f, 0.f);
+
+    for (int64_t r0 = sa; r0 < se; r0 += p.stage) {
+      const int nr = (int)((se - r0 < p.stage) ? se - r0 : p.stage);
+      // This lane's rows of the piece are rb, rb + RS, ... in groups of G;
+      // full groups run unguarded, a short last group repeats the lane's
+      // first row for its missing rows and skips them.
+      const int n = nr > rb ? (nr - rb + RS - 1) / RS : 0;
+      const int nfull = n / G, tail = n - nfull * G;
+      const uint32_t* wp[NR];  // this lane's words of row r0 + rb
 #pragma unroll
-      for (int m = 0; m < M; ++m) xr[m] = xs[rl * M + m];
-    }
-    float sr = 0.f;
-    if constexpr (BW) sr = scs[rl];
+      for (int i = 0; i < NR; ++i) wp[i] = base + (r0 + rb) * rowWords + ((wa + i >= WPB) ? wa + i - WPB : wa + i);
+      const int64_t rstep = (int64_t)RS * rowWords;  // words between this lane's consecutive rows
+      auto load_full = [&](uint32_t (&a)[G][NR], int64_t off) {
 #pragma unroll
-    for (int i2 = 0; i2 < 8; ++i2) {
-      float2 y = __fadd2_rn(
-          make_float2(__uint_as_float(code_magic(s[2 * i2])), __uint_as_float(code_magic(s[2 * i2 + 1]))), nmagic);
-      if constexpr (BW) {  // bf16(value * scale), the expand weight
-        const float2 wv = __fmul2_rn(value_rn2(y), make_float2(sr, sr));
-        const uint32_t bb = pack_bf16x2(wv.x, wv.y);
-        y = make_float2(bf16lo_to_f32(bb), bf16hi_to_f32(bb));
+        for (int u = 0; u < G; ++u)
+#pragma unroll
+          for (int q = 0; q < NR; ++q) a[u][q] = __ldg(wp[q] + off + u * rstep);
+      };
+      auto load_tail = [&](uint32_t (&a)[G][NR], int64_t off) {
+#pragma unroll
+        for (int u = 0; u < G; ++u) {
+          const int64_t o = u < tail ? off + u * rstep : 0;
+#pragma unroll
+          for (int q = 0; q < NR; ++q) a[u][q] = __ldg(wp[q] + o);
+        }
+      };
+      uint32_t A[G][NR], B[G][NR];
+      if (nfull > 0) load_full(A, 0);
+      else if (tail > 0) load_tail(A, 0);
+
+      // stage x*scale (or x and the scales) of the piece, four rows per thread in flight
+      for (int rr = threadIdx.x; rr < nr; rr += 4 * blockDim.x) {
+        float sv[4], xv[4][M];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int rl = rr + u * (int)blockDim.x;
+          const int64_t r = r0 + (rl < nr ? rl : 0);
+          sv[u] = f16_to_f32(__ldg(p.scales + r));
+#pragma unroll
+          for (int m = 0; m < M; ++m) xv[u][m] = bf16_to_f32(__ldg(p.x + (int64_t)m * p.R + r));
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int rl = rr + u * (int)blockDim.x;
+          if (rl < nr) {
+            // default numerics fold the row scale into x; bf16 weights need it per weight
+#pragma unroll
+            for (int m = 0; m < M; ++m) xs[rl * M + m] = BW ? xv[u][m] : __fmul_rn(xv[u][m], sv[u]);
+            if (BW) scs[rl] = sv[u];
+          }
+        }
       }
-#pragma unroll
-      for (int m = 0; m < M; ++m) acc[m][i2] = __ffma2_rn(y, make_float2(xr[m], xr[m]), acc[m][i2]);
-    }
-  };
-  auto run_chunk = [&](const uint32_t (&a)[kAx0Chunk][NR], int ch) {
-#pragma unroll
-    for (int u = 0; u < kAx0Chunk; ++u) {
-      const int i = ch * kAx0Chunk + u;
-      const int rl = row_of(i);
-      if (i < nw && rl < nr) body(a[u], rl);
-    }
-  };
-  for (int ch = 0; ch < nch; ch += 2) {
-    if (ch + 1 < nch) load_chunk(a1, ch + 1);
-    run_chunk(a0, ch);
-    if (ch + 1 >= nch) break;
-    if (ch + 2 < nch) load_chunk(a0, ch + 2);
-    run_chunk(a1, ch + 1);
-  }
+      __syncthreads();
 
-  // fold the two halves of each warp, then the warps of this CTA into red[0 .. M*256)
+    // one row: raw words, x of the row at xr[0..M), its scale at sc
+    auto body = [&](const uint32_t (&raw)[NR], const float* xr, const float* sc) {
+      uint32_t w[NR];
+      if constexpr (kEven) {
 #pragma unroll
-  for (int m = 0; m < M; ++m)
+        for (int i = 0; i < NR; ++i) w[i] = raw[i];
+      } else {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      acc[m][i].x += __shfl_xor_sync(0xFFFFFFFFu, acc[m][i].x, 16);
-      acc[m][i].y += __shfl_xor_sync(0xFFFFFFFFu, acc[m][i].y, 16);
+        for (int i = 0; i + 1 < NR; ++i) w[i] = __funnelshift_r(raw[i], raw[i + 1], sh);
+        w[NR - 1] = raw[NR - 1] >> sh;
+      }
+      uint32_t s[16];
+      run_states<K, L, 16, NR>(w, s);
+      float xv[M];
+      if constexpr (M == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(xr);
+        xv[0] = v.x; xv[1] = v.y; xv[2] = v.z; xv[3] = v.w;
+      } else {
+#pragma unroll
+        for (int m = 0; m < M; ++m) xv[m] = xr[m];
+      }
+      float sr = 0.f;
+      if constexpr (BW) sr = *sc;
+#pragma unroll
+      for (int i2 = 0; i2 < 8; ++i2) {
+        float2 y = __fadd2_rn(
+            make_float2(__uint_as_float(code_magic(s[2 * i2])), __uint_as_float(code_magic(s[2 * i2 + 1]))), nmagic);
+        if constexpr (BW) {  // bf16(value * scale), the expand weight
+          const float2 wv = __fmul2_rn(value_rn2(y), make_float2(sr, sr));
+          const uint32_t bb = pack_bf16x2(wv.x, wv.y);
+          y = make_float2(bf16lo_to_f32(bb), bf16hi_to_f32(bb));
+        }
+#pragma unroll
+        for (int m = 0; m < M; ++m) acc[m][i2] = __ffma2_rn(y, make_float2(xv[m], xv[m]), acc[m][i2]);
+      }
+    };
+      // group g covers this lane's rows g*G .. g*G+G-1
+      auto run_full = [&](const uint32_t (&a)[G][NR], int g) {
+        const float* xg = xs + (rb + g * G * RS) * M;
+        const float* sg = scs + rb + g * G * RS;
+#pragma unroll
+        for (int u = 0; u < G; ++u) body(a[u], xg + u * RS * M, sg + u * RS);
+      };
+      auto run_tail = [&](const uint32_t (&a)[G][NR], int g) {
+        const float* xg = xs + (rb + g * G * RS) * M;
+        const float* sg = scs + rb + g * G * RS;
+#pragma unroll
+        for (int u = 0; u < G; ++u)
+          if (u < tail) body(a[u], xg + u * RS * M, sg + u * RS);
+      };
+      // A holds group g at the top of each iteration
+      int g = 0;
+      for (; g + 1 < nfull; g += 2) {
+        load_full(B, (int64_t)(g + 1) * G * rstep);
+        run_full(A, g);
+        if (g + 2 < nfull) load_full(A, (int64_t)(g + 2) * G * rstep);
+        else if (g + 2 == nfull && tail > 0) load_tail(A, (int64_t)(g + 2) * G * rstep);
+        run_full(B, g + 1);
+      }
+      if (g < nfull) {  // one full group left, then perhaps the tail
+        if (tail > 0) load_tail(B, (int64_t)(g + 1) * G * rstep);
+        run_full(A, g);
+        if (tail > 0) run_tail(B, g + 1);
+      } else if (tail > 0) {
+        run_tail(A, g);
+      }
+      __syncthreads();  // the staged piece is no longer read
     }
-  if (half == 0) {
+
+    // fold the two halves of each warp, then the warps of this CTA
 #pragma unroll
-    for (int m = 0; m < M; ++m) {
-      float4* dst = reinterpret_cast<float4*>(red + (warp * M + m) * kT + 16 * j);
+    for (int m = 0; m < M; ++m)
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        dst[q] = make_float4(acc[m][2 * q].x, acc[m][2 * q].y, acc[m][2 * q + 1].x, acc[m][2 * q + 1].y);
+      for (int i = 0; i < 8; ++i) {
+        acc[m][i].x += __shfl_xor_sync(0xFFFFFFFFu, acc[m][i].x, 16);
+        acc[m][i].y += __shfl_xor_sync(0xFFFFFFFFu, acc[m][i].y, 16);
+      }
+    if (half == 0) {
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        float4* dst = reinterpret_cast<float4*>(red + (warp * M + m) * kT + 16 * j);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          dst[q] = make_float4(acc[m][2 * q].x, acc[m][2 * q].y, acc[m][2 * q + 1].x, acc[m][2 * q + 1].y);
+      }
     }
-  }
-  __syncthreads();
-  // red position m*256 + t holds block position t (output column cb*256 + t)
-  for (int i = threadIdx.x; i < M * kT; i += blockDim.x) {
-    float v = red[i];
+    __syncthreads();
+    // red[w][m][t] holds block position t (output column cb*256 + t)
+    float* slot = p.part + (int64_t)(c + cb) * M * kT;
+    for (int i = threadIdx.x; i < M * kT; i += blockDim.x) {
+      float v = red[i];
 #pragma unroll
-    for (int w = 1; w < kAx0Warps; ++w) v += red[w * M * kT + i];
-    red[i] = v;
-  }
-  // fold the cluster's CTAs (slices sl - rank .. sl - rank + kAx0Cluster - 1):
-  // CTA `rank` takes outputs [rank, rank + 1) * M*256/kAx0Cluster
-  cluster_sync();
-  {
-    constexpr int kShare = M * kT / kAx0Cluster;
-    const uint32_t rank = cluster_rank();
-    const int cl = sl / kAx0Cluster;
-    for (int i = threadIdx.x; i < kShare; i += blockDim.x) {
-      const int o = (int)rank * kShare + i;
-      const int m = o / kT, t = o - m * kT;
-      float v = 0.f;
-#pragma unroll
-      for (int q = 0; q < kAx0Cluster; ++q) v += ld_dsmem(red + o, (uint32_t)q);
-      p.part[((int64_t)cl * M + m) * p.C + (int64_t)cb * kT + t] = v;
+      for (int w = 1; w < W; ++w) v += red[w * M * kT + i];
+      slot[i] = v;
     }
-  }
-  cluster_sync();  // no CTA leaves while another still reads its shared memory
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) last_flag = (atomicAdd(p.counter + cb, 1u) == (uint32_t)(p.S - 1)) ? 1u : 0u;
-  __syncthreads();
-  if (!last_flag) return;
-  __threadfence();
-  const int ncl = p.S / kAx0Cluster;
-  for (int i = threadIdx.x; i < M * kT; i += blockDim.x) {
-    const int m = i / kT, t = i - m * kT;
-    const float* pp = p.part + (int64_t)m * p.C + (int64_t)cb * kT + t;
-    const int64_t stride = (int64_t)M * p.C;
-    float v = 0.f;
-    int s = 0;
-    for (; s + 8 <= ncl; s += 8) {
-      float q[8];
+    // Arrival is deferred: a range that crosses column blocks publishes all
+    // its partials with one fence at the end instead of one per segment.
+    if (threadIdx.x == 0) pend[npend] = cb;
+    if (++npend == kAx0MaxPending || f >= f1) {
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0)
+        for (int i = 0; i < npend; ++i) {
+          const int pc = pend[i];
+          const int first = ax0_cta_of((int64_t)pc * p.R, p.N, p.G);
+          const int last = ax0_cta_of((int64_t)pc * p.R + p.R - 1, p.N, p.G);
+          is_last[i] = (atomicAdd(p.counter + pc, 1u) == (uint32_t)(last - first)) ? 1u : 0u;
+        }
+      __syncthreads();
+      for (int i = 0; i < npend; ++i) {
+        if (!is_last[i]) continue;
+        // the last CTA to arrive folds the column block's partials in CTA order
+        __threadfence();
+        const int pc = pend[i];
+        const int first = ax0_cta_of((int64_t)pc * p.R, p.N, p.G);
+        const int ns = ax0_cta_of((int64_t)pc * p.R + p.R - 1, p.N, p.G) - first + 1;
+        const float* ps = p.part + (int64_t)(first + pc) * M * kT;
+        for (int e = threadIdx.x; e < M * kT; e += blockDim.x) {
+          float v = 0.f;
+          for (int s0 = 0; s0 < ns; s0 += 16) {
+            float q[16];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) q[u] = __ldcg(pp + (s + u) * stride);
+            for (int u = 0; u < 16; ++u) q[u] = (s0 + u < ns) ? __ldcg(ps + (int64_t)(s0 + u) * M * kT + e) : 0.f;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) v += q[u];
+            for (int u = 0; u < 16; ++u)
+              if (s0 + u < ns) v += q[u];
+          }
+          const int m = e / kT, t = e - m * kT;
+          uint16_t o;
+          asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(o) : "f"(BW ? v : __fmul_rn(v, kRcpD)));
+          p.out[(int64_t)m * p.C + (int64_t)pc * kT + t] = o;
+        }
+        if (threadIdx.x == 0) p.counter[pc] = 0u;
+      }
+      npend = 0;
     }
-    for (; s < ncl; ++s) v += __ldcg(pp + s * stride);
-    uint16_t o;
-    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(o) : "f"(BW ? v : __fmul_rn(v, kRcpD)));
-    p.out[(int64_t)m * p.C + (int64_t)cb * kT + t] = o;
+    __syncthreads();  // red, pend and is_last are reused by the next segment
   }
-  if (threadIdx.x == 0) p.counter[cb] = 0u;
 }
 
-template <int K, int L, int M, bool BW>
-static cudaError_t ax0_launch1(const Ax0Params& p, size_t smem, cudaStream_t st) {
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3((unsigned)p.nb, (unsigned)p.S);
-  cfg.blockDim = dim3(32 * kAx0Warps);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = kAx0Cluster;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, ax0_kernel<K, L, M, BW>, p);
+int ax0_sm_count() {
+  static std::mutex mu;
+  static int cached[64];
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[dev]) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+template <int K, int L, int M, bool BW, bool IL>
+static cudaError_t ax0_launch1(const Ax0Params& p, cudaStream_t st) {
+  constexpr int W = ax0_warps<M>();
+  const size_t smem = ((((size_t)p.stage * M + 3) & ~(size_t)3) + (size_t)W * M * kT + (BW ? (size_t)p.stage : 0)) *
+                      sizeof(float);
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    const size_t most = ((kAx0StageRows * M + 3) & ~(size_t)3) * sizeof(float) + (size_t)W * M * kT * sizeof(float) +
+                        (BW ? kAx0StageRows * sizeof(float) : 0);
+    attr_err = cudaFuncSetAttribute(ax0_kernel<K, L, M, BW, IL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  ax0_kernel<K, L, M, BW, IL><<<p.G, 32 * W, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <int K, int L, bool BW, bool IL>
+static cudaError_t ax0_launch_il(const Ax0Params& p, int M, cudaStream_t st) {
+  switch (M) {
+    case 1: return ax0_launch1<K, L, 1, BW, IL>(p, st);
+    case 2: return ax0_launch1<K, L, 2, BW, IL>(p, st);
+    case 3: return ax0_launch1<K, L, 3, BW, IL>(p, st);
+    default: return ax0_launch1<K, L, 4, BW, IL>(p, st);
+  }
 }
 
 template <int K, int L, bool BW>
-static cudaError_t ax0_launch_m(const Ax0Params& p, int M, cudaStream_t st) {
-  const size_t sm = ((((size_t)p.rps * M + 3) & ~(size_t)3) + (size_t)kAx0Warps * M * kT + (BW ? (size_t)p.rps : 0)) *
-                    sizeof(float);
-  cudaError_t e;
-  switch (M) {
-    case 1: e = ax0_launch1<K, L, 1, BW>(p, sm, st); break;
-    case 2: e = ax0_launch1<K, L, 2, BW>(p, sm, st); break;
-    case 3: e = ax0_launch1<K, L, 3, BW>(p, sm, st); break;
-    default: e = ax0_launch1<K, L, 4, BW>(p, sm, st); break;
-  }
-  return e != cudaSuccess ? e : cudaGetLastError();
+static cudaError_t ax0_launch_m(const Ax0Params& p, int M, bool il, cudaStream_t st) {
+  if constexpr (K == 3)  // the interleaved layout exists for k = 3 only
+    if (il) return ax0_launch_il<K, L, BW, true>(p, M, st);
+  return ax0_launch_il<K, L, BW, false>(p, M, st);
 }
 
 template <bool BW>
 static cudaError_t ax0_dispatch(const uint32_t* codes, const uint16_t* scales, const uint16_t* x, uint16_t* out, int M,
                                 int k, int L, int64_t rows, int64_t cols, int interleave, void* workspace,
                                 cudaStream_t st) {
-  const Ax0Plan pl = ax0_plan(rows, cols);
-  if (pl.S > 65535) return cudaErrorInvalidConfiguration;  // grid y limit (more than 10^8 stored rows)
   Ax0Params p{};
   p.codes = codes; p.scales = scales; p.x = x; p.out = out;
+  p.nb = (int)(cols / kT);
   p.part = static_cast<float*>(workspace);
-  p.counter = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + (size_t)(pl.S / kAx0Cluster) * (size_t)M *
-                                                                              (size_t)cols * sizeof(float));
-  p.R = rows; p.C = cols; p.rps = pl.rps; p.nb = pl.nb; p.S = pl.S; p.interleave = interleave;
+  p.counter = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) +
+                                          (size_t)(kAx0MaxCtas + p.nb) * (size_t)M * kT * sizeof(float));
+  p.R = rows; p.C = cols; p.N = (int64_t)p.nb * rows;
+  int64_t G = ax0_sm_count();
+  if (G > kAx0MaxCtas) G = kAx0MaxCtas;
+  if (G > (p.N + kAx0MinRows - 1) / kAx0MinRows) G = (p.N + kAx0MinRows - 1) / kAx0MinRows;
+  if (G < 1) G = 1;
+  p.G = (int)G;
+  const int64_t per = (p.N + G - 1) / G;  // longest range, hence longest segment
+  p.stage = (int)(per < kAx0StageRows ? per : kAx0StageRows);
+  const bool il = interleave != 0;
   if (L == 16) {
-    if (k == 2) return ax0_launch_m<2, 16, BW>(p, M, st);
-    if (k == 3) return ax0_launch_m<3, 16, BW>(p, M, st);
-    return ax0_launch_m<4, 16, BW>(p, M, st);
+    if (k == 2) return ax0_launch_m<2, 16, BW>(p, M, il, st);
+    if (k == 3) return ax0_launch_m<3, 16, BW>(p, M, il, st);
+    return ax0_launch_m<4, 16, BW>(p, M, il, st);
   }
-  if (k == 2) return ax0_launch_m<2, 12, BW>(p, M, st);
-  if (k == 3) return ax0_launch_m<3, 12, BW>(p, M, st);
-  return ax0_launch_m<4, 12, BW>(p, M, st);
+  if (k == 2) return ax0_launch_m<2, 12, BW>(p, M, il, st);
+  if (k == 3) return ax0_launch_m<3, 12, BW>(p, M, il, st);
+  return ax0_launch_m<4, 12, BW>(p, M, il, st);
 }
 
 cudaError_t launch_matvec_axis0(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
