@@ -121,8 +121,14 @@ def check_gateup(oracle, gpu_bits, gref, gab, uref, uab, what):
     """Accept an output if it is within one bf16 ulp of the activation chain
     evaluated at some pair of bf16 gate/up values that a correctly rounded
     cast of sums inside the tolerance band can give.  Returns the fraction of
-    outputs whose gate or up band held more than one bf16 value."""
-    from util import ABS_TOL, REL_TOL, _ordered, bf16_of_f64
+    outputs whose gate or up band held more than one bf16 value.
+
+    The band ends and the reference itself are tried first.  An output they
+    do not explain is checked against every bf16 gate value of its band: for
+    a fixed gate the chain bf16(silu(g) * u) is monotone in u and moves by at
+    most two ulps per bf16 step of u, so the outputs reachable over the up
+    band are those between the chain at its two ends, give or take one ulp."""
+    from util import ABS_TOL, REL_TOL, _bits_of_ordered, _ordered, bf16_of_f64
     tg, tu = REL_TOL * gab + ABS_TOL, REL_TOL * uab + ABS_TOL
     cands_g = [bf16_of_f64(oracle, gref - tg), bf16_of_f64(oracle, gref), bf16_of_f64(oracle, gref + tg)]
     cands_u = [bf16_of_f64(oracle, uref - tu), bf16_of_f64(oracle, uref), bf16_of_f64(oracle, uref + tu)]
@@ -132,6 +138,13 @@ def check_gateup(oracle, gpu_bits, gref, gab, uref, uab, what):
         for cu in cands_u:
             want = _ordered(oracle.swiglu_bf16(cg, cu))
             ok |= np.abs(gpu - want) <= 1
+    glo, ghi = _ordered(cands_g[0]), _ordered(cands_g[2])
+    for idx in zip(*np.nonzero(~ok)):
+        gvals = np.arange(glo[idx], ghi[idx] + 1)
+        gbits = _bits_of_ordered(gvals)
+        a = _ordered(oracle.swiglu_bf16(gbits, np.full(gbits.shape, cands_u[0][idx], dtype=np.uint16)))
+        b = _ordered(oracle.swiglu_bf16(gbits, np.full(gbits.shape, cands_u[2][idx], dtype=np.uint16)))
+        ok[idx] = bool(((gpu[idx] >= np.minimum(a, b) - 1) & (gpu[idx] <= np.maximum(a, b) + 1)).any())
     assert ok.all(), f"{what}: {int((~ok).sum())} of {ok.size} outputs off the chain"
     multi = (cands_g[0] != cands_g[2]) | (cands_u[0] != cands_u[2])
     return float(multi.mean())

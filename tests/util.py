@@ -50,6 +50,12 @@ def _ordered(bits: np.ndarray) -> np.ndarray:
     return np.where(b & 0x8000, -(b & 0x7FFF), b)
 
 
+def _bits_of_ordered(o: np.ndarray) -> np.ndarray:
+    """Inverse of _ordered (zero maps to +0)."""
+    o = np.asarray(o).astype(np.int32)
+    return np.where(o < 0, (-o) | 0x8000, o).astype(np.uint16)
+
+
 def check_band(oracle, gpu_bits: np.ndarray, ref: np.ndarray, absum: np.ndarray, what: str = ""):
     """Assert the tolerance rule for every element; return the max |ulp| distance."""
     gpu_bits = np.asarray(gpu_bits, dtype=np.uint16)

@@ -76,6 +76,22 @@ __device__ __forceinline__ float f16_to_f32(uint16_t h) {
   return f;
 }
 
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
+  uint16_t r;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(v));
+  return r;
+}
+
+// The SwiGLU cast chain of GATEUP_SOURCE ("trellis-linear.ts" diff page) on
+// fp32 gate/up sums: each intermediate is rounded to bf16.
+__device__ __forceinline__ uint16_t swiglu_chain(float gate, float up) {
+  const float g = bf16_to_f32(f32_to_bf16_rn(gate));
+  const float u = bf16_to_f32(f32_to_bf16_rn(up));
+  const float sig = bf16_to_f32(f32_to_bf16_rn(__fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-g)))));
+  const float silu = bf16_to_f32(f32_to_bf16_rn(__fmul_rn(g, sig)));
+  return f32_to_bf16_rn(__fmul_rn(silu, u));
+}
+
 // The L-bit window starting at run-relative bit O of the words w[] (w[0]
 // holds run bits 0..31).  O is a compile-time constant after unrolling.
 template <int L, int NW>

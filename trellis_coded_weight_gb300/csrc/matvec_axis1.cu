@@ -42,21 +42,6 @@ struct Mv1Params {
   int nb;      // blocks per row (C / 256)
 };
 
-__device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
-  uint16_t r;
-  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(v));
-  return r;
-}
-
-// The SwiGLU cast chain of GATEUP_SOURCE on fp32 gate/up sums.
-__device__ __forceinline__ uint16_t swiglu_chain(float gate, float up) {
-  const float g = bf16_to_f32(f32_to_bf16_rn(gate));
-  const float u = bf16_to_f32(f32_to_bf16_rn(up));
-  const float sig = bf16_to_f32(f32_to_bf16_rn(__fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-g)))));
-  const float silu = bf16_to_f32(f32_to_bf16_rn(__fmul_rn(g, sig)));
-  return f32_to_bf16_rn(__fmul_rn(silu, u));
-}
-
 // A half block: runs 7..4 (block words [0, 4K)) or runs 3..0 (words
 // [4K, 8K)), plus the spill word of its last run (word 4K, or word 0 where
 // the block wraps).
