@@ -36,6 +36,17 @@ __device__ __forceinline__ float code_y(uint32_t s) {
   return __fsub_rn(__uint_as_float(code_magic(s)), kMagic);
 }
 
+// y as an integer (the byte sum onto -510), and as an exact float through an
+// int-to-float conversion.  The conversion runs on the ALU pipe, the bias
+// subtraction of code_magic on the FMA pipe that also carries the 1MAD
+// multiply and the byte sum, so kernels bound by that pipe use this form.
+__device__ __forceinline__ int code_int(uint32_t s) {
+  return (int)__dp4a(s * kMulA + kAddB, 0x01010101u, (uint32_t)-510);
+}
+__device__ __forceinline__ float2 code_y2_alu(uint32_t s0, uint32_t s1) {
+  return make_float2(__int2float_rn(code_int(s0)), __int2float_rn(code_int(s1)));
+}
+
 // Correctly rounded y / d: the reciprocal product refined by one residual
 // step ("trellis_val_rcp" in the HEADER source).  The pages state, and the
 // oracle pins check exhaustively, that this equals the IEEE quotient for

@@ -19,8 +19,9 @@
 //   * x is staged per block as fp32 in shared memory and read with broadcast
 //     128-bit loads (every lane of the warp reads the same address), so the
 //     x traffic costs one shared-memory wavefront per 4 positions x 32 rows.
-//   * the 1MAD byte sum is one dp4a onto a float bias, y = float - bias with
-//     packed f32x2 arithmetic, and y*x accumulates with packed f32x2 FMA; the
+//   * the 1MAD byte sum is one dp4a onto -510 and y an int-to-float
+//     conversion (ALU pipe, leaving the FMA-heavy pipe to the multiply, the
+//     byte sum and the FMAs), and y*x accumulates with packed f32x2 FMA; the
 //     per-row factor scale/d is applied once after the reduction (the pages
 //     apply it per weight; the difference is a few fp32 ulp per sum).
 //   * each decoded weight is shared across the M input rows.
@@ -91,7 +92,6 @@ __global__ void __launch_bounds__(512) mv1_kernel(const Mv1Params p) {
   for (int t = 0; t < NMAT; ++t)
 #pragma unroll
     for (int m = 0; m < M; ++m) acc[t][m][0] = acc[t][m][1] = make_float2(0.f, 0.f);
-  const float2 nmagic = make_float2(-kMagic, -kMagic);
   // bf16-weight numerics: each weight is bf16(value * scale) before the FMA
   float wsc[NMAT];
 #pragma unroll
@@ -127,10 +127,8 @@ __global__ void __launch_bounds__(512) mv1_kernel(const Mv1Params p) {
         run_states<K, L>(w, s);
 #pragma unroll
         for (int j4 = 0; j4 < 8; ++j4) {
-          float2 ya = __fadd2_rn(make_float2(__uint_as_float(code_magic(s[4 * j4])),
-                                             __uint_as_float(code_magic(s[4 * j4 + 1]))), nmagic);
-          float2 yb = __fadd2_rn(make_float2(__uint_as_float(code_magic(s[4 * j4 + 2])),
-                                             __uint_as_float(code_magic(s[4 * j4 + 3]))), nmagic);
+          float2 ya = code_y2_alu(s[4 * j4], s[4 * j4 + 1]);
+          float2 yb = code_y2_alu(s[4 * j4 + 2], s[4 * j4 + 3]);
           if constexpr (BW) {
             ya = bf16_weights(ya, wsc[t]);
             yb = bf16_weights(yb, wsc[t]);

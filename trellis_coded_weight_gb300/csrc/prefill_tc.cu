@@ -23,11 +23,13 @@
 //               reads its own 32-lane sub-partition), bf16 conversion and
 //               coalesced stores of out[m][r].  With two accumulators (BN <=
 //               256) the epilogue of one tile overlaps the next tile's MMAs.
-//   warps 6-21  decoders in groups that take turns on the ring's stages:
+//   warps 6-21  decoders in groups that take turns on the ring's stages
+//               (axis 1: on half blocks of 128 columns, each thread loading
+//               its row's half block once with 16-byte loads):
 //               each thread decodes a run of 32 positions of one of the
 //               tile's 128 weight rows straight into the swizzled A tile
 //               (generic-proxy stores, then fence.proxy.async).  The code
-//               words of a run are loaded two turns ahead.
+//               words of the next turn load while the current turn decodes.
 // Tile shapes: BN = 512 tokens for M > 256 (a 512-column accumulator, so each
 // decoded weight feeds 512 tokens -- decoding, not the tensor core, is the
 // costly part of this GEMM), else the smallest of 32..256 that covers M.
@@ -166,6 +168,24 @@ __device__ __forceinline__ void decode_col_to_tile(const uint32_t* ct, int row0,
 
 __device__ __forceinline__ void report(int code) { atomicCAS(&g_device_error, 0, code); }
 
+// Axis 1: the K order of a tile's nk stages.  Half blocks of 128 columns
+// (SPH stages each) go to the NG decoder groups in turn; within a round of NG
+// half blocks the stages interleave the groups (stage = round base + r*NG +
+// group, r = the run index of the half block), so a decoder thread loads a
+// half block once and every group's next stage is at most NG stages after
+// its last -- never a full lap of the stage ring ahead of the MMAs.  The
+// half blocks past the last full round go stage by stage to the groups in
+// turn.  Returns the first column of stage ks.
+template <int SPH, int NG, int BK>
+__device__ __forceinline__ int ax1_stage_col(int ks, int nk) {
+  const int full = (nk / SPH / NG) * NG * SPH;
+  if (ks < full) {
+    const int T = ks / (NG * SPH), rem = ks % (NG * SPH);
+    return (T * NG + rem % NG) * 128 + (rem / NG) * BK;
+  }
+  return (full / SPH + (ks - full) / SPH) * 128 + ((ks - full) % SPH) * BK;
+}
+
 template <int K, int L, int BN, int BK, int AX>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_out,
@@ -237,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int h = 0; h < NH; ++h)
             tc::tma_load_2d(b_tiles + (size_t)s * C_::BTile + (size_t)h * NMMA * RowBytes, &tmap_x, full_b + s,
-                            ks * BK, m0 + h * NMMA);
+                            AX == 1 ? ax1_stage_col<128 / BK, C_::Groups, BK>(ks, nk) : ks * BK, m0 + h * NMMA);
           ++issued;
         }
       }
@@ -366,16 +386,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) tc::mbar_arrive(full_a + s);
       }
     } else {
-      auto fetch = [&](RunWords<K>& rw, int64_t g) {
-        if (g >= total) return;
-        const int lt = (int)(g / nk), ks = (int)(g % nk);
+      // Stage order of ax1_stage_col: a turn of this group is a half block of
+      // a full round (SPH stages, NG apart) or one stage past the last full
+      // round.  Each thread loads its row's half block once per turn with
+      // 16-byte loads, a turn ahead, and decodes its run of each stage from
+      // registers.  Words [4K, 8K) of a block hold runs 3..0 (positions
+      // 0..127) with the spill word 0; words [0, 4K) hold runs 7..4 with the
+      // spill word 4K.
+      constexpr int SPH = 128 / BK;  // stages per half block
+      constexpr int RPR = C_::RunsPerRow;
+      static_assert(NG <= NS, "a group's consecutive stages must stay within one lap of the ring");
+      const int F = nk / SPH / NG, full = F * NG * SPH;
+      const int tail = nk - full > grp ? (nk - full - grp + NG - 1) / NG : 0;  // this group's stages past the rounds
+      const int per_tile = F + tail;
+      const int64_t nturn = (int64_t)n_local * per_tile;
+      struct HalfWords {
+        uint32_t w[4 * K + 1];
+        float scale;
+      };
+      // turn u: tile lt, half block hbk, first stage ks0 (full turns: SPH stages NG apart; tail: one stage of run r0)
+      auto turn = [&](int64_t u, int& lt, int& hbk, int& ks0, int& r0) -> bool {
+        lt = (int)(u / per_tile);
+        const int v = (int)(u % per_tile);
+        if (v < F) {
+          hbk = v * NG + grp; ks0 = v * NG * SPH + grp; r0 = -1;
+          return true;
+        }
+        ks0 = full + grp + (v - F) * NG;
+        hbk = F * NG + (ks0 - full) / SPH; r0 = (ks0 - full) % SPH;
+        return false;
+      };
+      auto fetch = [&](HalfWords& hw, int64_t u) {
+        if (u >= nturn) return;
+        int lt, hbk, ks0, r0;
+        turn(u, lt, hbk, ks0, r0);
         const int t = (int)blockIdx.x + lt * G;
         int64_t r = (int64_t)(t % p.nRT) * kBM + rl;
         if (r >= p.R) r = p.R - 1;  // rows past the end decode row R-1 and are never stored
-        const int c = ks * BK + 32 * h;  // first column of the run
-        load_run<K>(rw, p.codes + (r * p.nb + c / kT) * WPB, (c % kT) / 32, p.scales + r);
+        const int c0 = hbk * 128;   // first column of the half block
+        const int hb = (c0 % kT) < 128 ? 1 : 0;
+        const uint32_t* blk = p.codes + (r * p.nb + c0 / kT) * WPB;
+        const uint4* v4 = reinterpret_cast<const uint4*>(blk + hb * 4 * K);
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+          const uint4 v = __ldg(v4 + i);
+          hw.w[4 * i] = v.x; hw.w[4 * i + 1] = v.y; hw.w[4 * i + 2] = v.z; hw.w[4 * i + 3] = v.w;
+        }
+        hw.w[4 * K] = __ldg(blk + (hb ? 0 : 4 * K));
+        hw.scale = f16_to_f32(__ldg(p.scales + r));
       };
-      auto process = [&](const RunWords<K>& rw, int64_t g) -> bool {
+      // one stage: decode run qh (of the half block) into slot g % NS
+      auto stage = [&](const RunWords<K>& rw, int64_t g) -> bool {
         const int s = (int)(g % NS);
         if (g >= NS && !tc::mbar_wait(empty + s, (uint32_t)((g / NS) & 1) ^ 1u, kWaitNs)) return false;
         decode_run_to_tile<K, L>(rw, a_tiles + (size_t)s * C_::ATile + rl * RowBytes, sw, 4 * h);
@@ -384,18 +445,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) tc::mbar_arrive(full_a + s);
         return true;
       };
-      RunWords<K> ra, rb;
-      int64_t g = grp;
-      fetch(ra, g);
-      fetch(rb, g + NG);
-      while (g < total) {
-        if (!process(ra, g)) { *fail = 1; break; }
-        fetch(ra, g + 2 * NG);
-        g += NG;
-        if (g >= total) break;
-        if (!process(rb, g)) { *fail = 1; break; }
-        fetch(rb, g + 2 * NG);
-        g += NG;
+      auto process = [&](const HalfWords& hw, int64_t u) -> bool {
+        int lt, hbk, ks0, r0;
+        const bool round = turn(u, lt, hbk, ks0, r0);
+        const int64_t gbase = (int64_t)lt * nk + ks0;
+        if (round) {
+#pragma unroll
+          for (int ss = 0; ss < SPH; ++ss) {  // run qh = ss*RPR + h, at words (3-qh)*K
+            RunWords<K> rw;
+#pragma unroll
+            for (int i = 0; i <= K; ++i) {
+              if constexpr (RPR > 1) rw.w[i] = h ? hw.w[(2 - ss * RPR) * K + i] : hw.w[(3 - ss * RPR) * K + i];
+              else rw.w[i] = hw.w[(3 - ss) * K + i];
+            }
+            rw.scale = hw.scale;
+            if (!stage(rw, gbase + (int64_t)ss * NG)) return false;
+          }
+          return true;
+        }
+        RunWords<K> rw;  // one stage of run r0: select its words
+#pragma unroll
+        for (int i = 0; i <= K; ++i) {
+          uint32_t v = 0;
+#pragma unroll
+          for (int rr = 0; rr < SPH; ++rr)
+#pragma unroll
+            for (int hh = 0; hh < RPR; ++hh)
+              if (rr == r0 && hh == h) v = hw.w[(3 - rr * RPR - hh) * K + i];
+          rw.w[i] = v;
+        }
+        rw.scale = hw.scale;
+        return stage(rw, gbase);
+      };
+      HalfWords ha, hb2;
+      int64_t u = 0;
+      fetch(ha, 0);
+      fetch(hb2, 1);
+      while (u < nturn) {
+        if (!process(ha, u)) { *fail = 1; break; }
+        fetch(ha, u + 2);
+        if (++u >= nturn) break;
+        if (!process(hb2, u)) { *fail = 1; break; }
+        fetch(hb2, u + 2);
+        ++u;
       }
     }
   }
