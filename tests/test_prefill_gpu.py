@@ -76,6 +76,17 @@ def test_prefill_axis0_small(oracle_mod, k, M, rows, cols):
     check_band(oracle_mod, bf16_bits(out), ref, ab, f"prefill axis0 k={k} M={M} {rows}x{cols}")
 
 
+def test_prefill_axis0_split_is_deterministic():
+    # 4 output tiles leave SMs idle, so each tile's 1000-row reduction is split over a cluster of CTAs
+    # whose partial accumulators are summed in a fixed CTA order: repeated calls give identical bits.
+    codes, scales, x = inputs.make_linear(1000, 512, 3, 300, seed_codes=7, seed_x=8, sigma=0.5, x_len=1000)
+    g = tb.Geometry(3, L, T, 0, 1000, 512)
+    dc, ds, dx = to_dev_u32(codes), to_dev_f16(scales), to_dev_bf16(x)
+    first = tb.gemm_prefill(dc, ds, dx, g)
+    for _ in range(3):
+        assert torch.equal(tb.gemm_prefill(dc, ds, dx, g).view(torch.int16), first.view(torch.int16))
+
+
 @pytest.mark.parametrize("M", [64, 512])
 def test_prefill_axis0_full_size_sampled(oracle_mod, M):
     rows, cols, k = 17408, 5120, 3

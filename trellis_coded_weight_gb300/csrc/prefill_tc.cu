@@ -33,6 +33,9 @@
 // Tile shapes: BN = 512 tokens for M > 256 (a 512-column accumulator, so each
 // decoded weight feeds 512 tokens -- decoding, not the tensor core, is the
 // costly part of this GEMM), else the smallest of 32..256 that covers M.
+// Axis 0 with fewer output tiles than SMs: a thread-block cluster of S CTAs
+// splits each tile's reduction and sums the partial accumulators through
+// distributed shared memory (epilogue, split reduction).
 #include <cstdint>
 #include <cstring>
 #include <cuda.h>
@@ -67,7 +70,10 @@ struct PrefillParams {
   int M, nb;
   int nRT, nTiles;  // output-feature tiles, total tiles
   int tma_out;      // 1: out written by TMA tensor stores (nOut % 8 == 0)
+  int S;            // axis 0: CTAs (a cluster) splitting each tile's reduction; 1 = no split
 };
+
+constexpr int kMaxChunks = 16;  // 32-column chunks of the widest accumulator (BN = 512)
 
 // CT: bytes of the per-stage code tile (axis 0 only; 0 for axis 1).
 template <int BN, int BK, int CT = 0>
@@ -81,7 +87,10 @@ struct Cfg {
   static constexpr int Stage = ATile + BTile + CTile;
   static constexpr int EpiBytes = kEpiWarps * 2 * 32 * 32 * 2;  // per warp: two 32x32 bf16 sub-tiles
   static constexpr int ScaleBytes = CT ? kDecWarps * 32 * 4 : 0;  // per-warp row scales (axis 0)
-  static constexpr int NS0 = (220 * 1024 - EpiBytes - ScaleBytes) / Stage;
+  // axis 0 split: two fp32 [32][128] chunk buffers, the first in the (then unused) bf16 epilogue staging
+  static constexpr int RedBytes = CT ? 32 * kBM * 4 : 0;
+  static_assert(EpiBytes == 32 * kBM * 4, "the epilogue staging holds one fp32 chunk");
+  static constexpr int NS0 = (220 * 1024 - EpiBytes - ScaleBytes - RedBytes) / Stage;
   static constexpr int NS = NS0 > 8 ? 8 : NS0;         // ring stages
   static constexpr int TmemCols = NACC * BN < 32 ? 32 : NACC * BN;
   static constexpr int RunsPerRow = BK / 32;            // runs of 32 positions per row and stage
@@ -90,9 +99,12 @@ struct Cfg {
   static constexpr uint32_t SBO = 8u * BK * 2u;         // bytes between 8-row groups
   static constexpr uint32_t SwMode = BK == 64 ? 2u : 4u;  // descriptor swizzle: 128B or 64B
   static constexpr CUtensorMapSwizzle TmaSw = BK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-  static constexpr size_t Smem = 1024 + (size_t)NS * Stage + EpiBytes + ScaleBytes + 512;
+  static constexpr size_t Smem = 1024 + (size_t)NS * Stage + EpiBytes + ScaleBytes + RedBytes + 1024;
   static_assert(BK == 64 || BK == 32, "stage width");
   static_assert(NS >= 2, "ring too small");
+  // a decoder group's consecutive stages are Groups apart: within one lap of the ring, so that an
+  // mbarrier parity never stands for a phase two laps old
+  static_assert(Groups <= NS, "decoder groups must not outnumber the ring's stages");
 };
 
 // The words of one run (K words of positions 32q .. 32q+31 plus the spill
@@ -203,7 +215,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* c_tiles = b_tiles + (size_t)NS * C_::BTile;   // NS x CTile (axis 0: code words of the stage)
   uint8_t* epi_stage = smem + (size_t)NS * C_::Stage;     // kEpiWarps x 2 x [32 tokens][32 rows] bf16
   float* sbuf = reinterpret_cast<float*>(epi_stage + C_::EpiBytes);  // axis 0: 32 row scales per decoder warp
-  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_stage + C_::EpiBytes + C_::ScaleBytes);
+  // axis 0 split: chunk buffer 0 is the epilogue staging, buffer 1 follows the row scales; [32][128] fp32 each
+  float* red[2] = {reinterpret_cast<float*>(epi_stage),
+                   reinterpret_cast<float*>(epi_stage + C_::EpiBytes + C_::ScaleBytes)};
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_stage + C_::EpiBytes + C_::ScaleBytes + C_::RedBytes);
   uint64_t* full_a = bars;                 // decoder group -> MMA
   uint64_t* full_b = bars + NS;            // TMA -> MMA (1 arrival + tx bytes)
   uint64_t* empty = bars + 2 * NS;         // MMA commit -> producer and decoders
@@ -211,12 +226,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_empty = bars + 3 * NS + 2; // [NACC] epilogue warps -> MMA
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * NS + 4);
   volatile int* fail = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint64_t* ready = bars + 3 * NS + 5;              // [kMaxChunks] split: partials of a chunk -> its owner
+  uint64_t* done = bars + 3 * NS + 5 + kMaxChunks;  // [kMaxChunks] split: the owner has read a chunk
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = gridDim.x;
-  const int n_local = (p.nTiles - (int)blockIdx.x + G - 1) / G;
+  // Without a split a CTA walks tiles cid, cid + G, ... over all nk stages.  With a split (axis 0), the S
+  // CTAs of a cluster share one tile and CTA `rank` runs stages [kbeg, kbeg + kcnt) of its reduction.
+  const bool split = AX == 0 && p.S > 1;
+  const int S = split ? p.S : 1;
+  const int G = gridDim.x / S;
+  const int cid = (int)blockIdx.x / S, rank = (int)blockIdx.x % S;
+  const int n_local = (p.nTiles - cid + G - 1) / G;
   const int nk = (int)((p.Kd + BK - 1) / BK);  // the last stage may run past Kd: TMA fills zeros
-  const int64_t total = (int64_t)n_local * nk;  // stages this CTA runs
+  const int kbeg = (int)((int64_t)rank * nk / S);
+  const int kcnt = (int)((int64_t)(rank + 1) * nk / S) - kbeg;
+  const int64_t total = (int64_t)n_local * kcnt;  // stages this CTA runs
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -228,6 +252,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(acc_full + b, 1);
       tc::mbar_init(acc_empty + b, kEpiWarps);
     }
+    if (split)
+      for (int i = 0; i < kMaxChunks; ++i) {
+        tc::mbar_init(ready + i, kEpiWarps * S);
+        tc::mbar_init(done + i, kEpiWarps);
+      }
     *fail = 0;
     tc::fence_mbar_init();
   }
@@ -238,6 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc::fence_before_sync();
   __syncthreads();
+  if (split) tc::cluster_sync_all();  // every CTA's barriers exist before any remote arrival
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
@@ -245,19 +275,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int64_t g = 0, issued = 0;
       for (int lt = 0; lt < n_local && !*fail; ++lt) {
-        const int t = (int)blockIdx.x + lt * G;
+        const int t = cid + lt * G;
         const int m0 = (t / p.nRT) * BN;
-        for (int ks = 0; ks < nk; ++ks, ++g) {
+        for (int ks = 0; ks < kcnt; ++ks, ++g) {
           const int s = (int)(g % NS);
           if (g >= NS && !tc::mbar_wait(empty + s, (uint32_t)((g / NS) & 1) ^ 1u, kWaitNs)) { *fail = 1; break; }
           tc::mbar_arrive_expect_tx(full_b + s, (uint32_t)(C_::BTile + C_::CTile));
           if constexpr (AX == 0)  // the codes of this stage's stored rows, for the tile's block
             tc::tma_load_2d(c_tiles + (size_t)s * C_::CTile, &tmap_codes, full_b + s, ((t % p.nRT) >> 1) * WPB,
-                            ks * BK);
+                            (kbeg + ks) * BK);
 #pragma unroll
           for (int h = 0; h < NH; ++h)
             tc::tma_load_2d(b_tiles + (size_t)s * C_::BTile + (size_t)h * NMMA * RowBytes, &tmap_x, full_b + s,
-                            AX == 1 ? ax1_stage_col<128 / BK, C_::Groups, BK>(ks, nk) : ks * BK, m0 + h * NMMA);
+                            AX == 1 ? ax1_stage_col<128 / BK, C_::Groups, BK>(ks, nk) : (kbeg + ks) * BK,
+                            m0 + h * NMMA);
           ++issued;
         }
       }
@@ -276,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_after_sync();
         const uint32_t d = tmem + (uint32_t)(buf * BN);
         bool ok = true;
-        for (int ks = 0; ks < nk; ++ks, ++g) {
+        for (int ks = 0; ks < kcnt; ++ks, ++g) {
           const int s = (int)(g % NS);
           const uint32_t ph = (uint32_t)((g / NS) & 1);
           if (!tc::mbar_wait(full_a + s, ph, kWaitNs) || !tc::mbar_wait(full_b + s, ph, kWaitNs)) { ok = false; break; }
@@ -295,6 +326,66 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mma_commit(acc_full + buf);
       }
     }
+  } else if (warp < kEpiWarp0 + kEpiWarps && split) {
+    // ---------------- epilogue, split reduction (axis 0) ----------------
+    // The cluster's S CTAs hold partial accumulators of one tile.  Chunk i
+    // (32 columns) is summed by CTA i % S: every CTA writes its partial of
+    // the chunk, fp32 [32 columns][128 rows], into its buffer i % 2 and
+    // arrives on the owner's ready[i]; the owner reads the S partials through
+    // distributed shared memory in rank order, stores bf16 and arrives on
+    // every CTA's done[i], which frees that buffer for chunk i + 2.  All
+    // barriers are single-use; no CTA leaves before the owners of its last
+    // two chunks are done with its buffers.
+    const int sp = warp & 3;
+    const int t = cid;
+    const int64_t rbase = (int64_t)(t % p.nRT) * kBM + 32 * sp;
+    const int64_t row = rbase + lane;
+    const int m0 = (t / p.nRT) * BN;
+    constexpr int NCH = BN / 32;
+    bool ok = __all_sync(0xffffffffu, tc::mbar_wait(acc_full, 0u, kWaitNs));
+    tc::fence_after_sync();
+    for (int i = 0; i < NCH && ok; ++i) {
+      const int b = i & 1, owner = i % S;
+      float* mine = red[b];
+      if (i >= 2 && !(ok = __all_sync(0xffffffffu, tc::mbar_wait_cluster(done + (i - 2), 0u, kWaitNs)))) break;
+      uint32_t v[32];
+      tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * sp) << 16) + (uint32_t)(32 * i), v);
+      tc::tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) mine[j * kBM + 32 * sp + lane] = __uint_as_float(v[j]);
+      tc::fence_acq_rel_cluster();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_cluster(ready + i, (uint32_t)owner);
+      if (rank == owner) {
+        if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait_cluster(ready + i, 0u, kWaitNs)))) break;
+        float acc[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+        for (int r = 0; r < S; ++r) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) acc[j] += tc::ld_dsmem_f32(mine + j * kBM + 32 * sp + lane, (uint32_t)r);
+        }
+        if (row < p.nOut) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int m = m0 + 32 * i + j;
+            if (m < p.M) {
+              uint16_t o;
+              asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(o) : "f"(acc[j]));
+              p.out[(int64_t)m * p.nOut + row] = o;
+            }
+          }
+        }
+        tc::fence_acq_rel_cluster();
+        __syncwarp();
+        if (lane == 0)
+          for (int r = 0; r < S; ++r) tc::mbar_arrive_cluster(done + i, (uint32_t)r);
+      }
+    }
+    // the owners of this CTA's last two chunks have read its buffers (waited even after a failure)
+    for (int i = (NCH > 2 ? NCH - 2 : 0); i < NCH; ++i)
+      if (!__all_sync(0xffffffffu, tc::mbar_wait_cluster(done + i, 0u, kWaitNs))) ok = false;
+    if (!ok) *fail = 1;
   } else if (warp < kEpiWarp0 + kEpiWarps) {
     // ---------------- epilogue ----------------
     const int sp = warp & 3;  // TMEM sub-partition this warp may read
@@ -304,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(acc_full + buf, (uint32_t)(use & 1), kWaitNs));
       tc::fence_after_sync();
       if (!ok) { *fail = 1; break; }
-      const int t = (int)blockIdx.x + lt * G;
+      const int t = cid + lt * G;
       const int64_t rbase = (int64_t)(t % p.nRT) * kBM + 32 * sp;  // first row of this warp's 32
       const int64_t row = rbase + lane;
       const int m0 = (t / p.nRT) * BN;
@@ -363,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* sb = sbuf + dw * 32;
       auto scale_of = [&](int64_t g) -> float {
         if (g >= total) return 0.f;
-        int64_t r = (int64_t)(g % nk) * BK + 32 * h + lane;
+        int64_t r = (int64_t)(kbeg + g % kcnt) * BK + 32 * h + lane;
         if (r >= p.R) r = p.R - 1;
         return f16_to_f32(__ldg(p.scales + r));
       };
@@ -377,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (g >= NS && !tc::mbar_wait(empty + s, ph ^ 1u, kWaitNs)) { *fail = 1; break; }
         if (!tc::mbar_wait(full_b + s, ph, kWaitNs)) { *fail = 1; break; }  // the code tile has landed
-        const int t = (int)blockIdx.x + (int)(g / nk) * G;
+        const int t = cid + (int)(g / kcnt) * G;
         const int tpos = (((t % p.nRT) * kBM) & (kT - 1)) + rl;  // position of this feature in its block
         decode_col_to_tile<K, L>(reinterpret_cast<const uint32_t*>(c_tiles + (size_t)s * C_::CTile), 32 * h, tpos,
                                  sb, a_tiles + (size_t)s * C_::ATile + rl * RowBytes, sw, 4 * h);
@@ -420,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (u >= nturn) return;
         int lt, hbk, ks0, r0;
         turn(u, lt, hbk, ks0, r0);
-        const int t = (int)blockIdx.x + lt * G;
+        const int t = cid + lt * G;
         int64_t r = (int64_t)(t % p.nRT) * kBM + rl;
         if (r >= p.R) r = p.R - 1;  // rows past the end decode row R-1 and are never stored
         const int c0 = hbk * 128;   // first column of the half block
@@ -571,6 +662,33 @@ cudaError_t prefill_launch(PrefillParams p, const uint16_t* x, cudaStream_t st) 
   p.nRT = (int)((p.nOut + kBM - 1) / kBM);
   p.nTiles = p.nRT * ((p.M + BN - 1) / BN);
   const int sms = sm_count();
+  // Axis 0 has few output tiles (one per 128 features): when they leave SMs idle, a cluster of S CTAs
+  // splits each tile's reduction (S <= 8, the portable cluster size, and S * tiles <= SMs).
+  int S = 1;
+  if (AX == 0) {
+    S = sms / p.nTiles;
+    if (S > 8) S = 8;
+    const int nk = (int)((p.Kd + BK - 1) / BK);
+    if (S > nk) S = nk;
+    if (S < 1) S = 1;
+  }
+  p.S = S;
+  if (S > 1) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)(p.nTiles * S));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C_::Smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, map, omap, cmap, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
   const int grid = p.nTiles < sms ? p.nTiles : sms;
   kern<<<grid, kThreads, C_::Smem, st>>>(map, omap, cmap, p);
   return cudaGetLastError();
