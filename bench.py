@@ -441,6 +441,9 @@ def run_single(kind: str, k: str, M: str):
     elif kind == "prefill":
         x = _dev_bf16(inputs.normal_bf16(inputs.SEED_X, (M, C)), dev)
         fn = lambda: tb.gemm_prefill(codes, sc, x, g1)
+    elif kind == "prefill0":  # axis-0 prefill: the stored W^T [R in][C out]
+        x = _dev_bf16(inputs.normal_bf16(inputs.SEED_X, (M, R), 0.5), dev)
+        fn = lambda: tb.gemm_prefill(codes, sc, x, g0)
     else:
         raise SystemExit(f"unknown kind {kind}")
     for _ in range(4):
@@ -481,7 +484,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--single", nargs=3, metavar=("KIND", "K", "M"),
                     help="profiling aid: run 4 launches of one kernel at full size and exit "
-                         "(KIND: axis1, gateup, axis0, expand, prefill)")
+                         "(KIND: axis1, gateup, axis0, expand, prefill, prefill0)")
     args = ap.parse_args()
     if args.single:
         run_single(*args.single)
