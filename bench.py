@@ -212,18 +212,39 @@ def run_gpu(args):
     value = world * step_bytes * args.steps / (ms_total * 1e-3) / 1e9
 
     # ---- end to end through the C ABI with host buffers (x in, out back) ----
+    # Every launch copies its x in from pinned host memory and its output back.  The copies run on
+    # their own streams so that they overlap the neighbouring launches: the x of each launch goes in
+    # ahead on the h2d stream, each output goes out on the d2h stream while the next launch runs.
+    # Each (k, M) slot has its own device buffers; events order the reuse of a slot across steps.
+    slots = [(k, M) for k in KS for M in MS]
     x_host = {M: xs[M].cpu().pin_memory() for M in MS}
-    o_host = {M: torch.empty((M, R), dtype=torch.bfloat16).pin_memory() for M in MS}
-    x_dev = {M: torch.empty_like(xs[M]) for M in MS}
+    o_host = {s: torch.empty((s[1], R), dtype=torch.bfloat16).pin_memory() for s in slots}
+    x_dev = {s: torch.empty_like(xs[s[1]]) for s in slots}
+    o_dev = {s: torch.empty((s[1], R), dtype=torch.bfloat16, device=dev) for s in slots}
+    h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = {s: {n: torch.cuda.Event() for n in ("h2d", "kern", "d2h")} for s in slots}
+    for s in slots:  # recorded once so that the first waits are satisfied
+        for e in ev[s].values():
+            e.record(stream)
 
     def e2e_step():
-        for k in KS:
-            for M in MS:
-                x_dev[M].copy_(x_host[M], non_blocking=True)
-                i = rot[k]
-                rot[k] = (i + 1) % len(bufs[k])
-                tb.matvec_axis1(bufs[k][i], scales[k], x_dev[M], geoms[k], outs[M])
-                o_host[M].copy_(outs[M], non_blocking=True)
+        with torch.cuda.stream(h2d_stream):
+            for s in slots:
+                h2d_stream.wait_event(ev[s]["kern"])  # the slot's previous launch has read its x
+                x_dev[s].copy_(x_host[s[1]], non_blocking=True)
+                ev[s]["h2d"].record(h2d_stream)
+        for s in slots:
+            k, M = s
+            stream.wait_event(ev[s]["h2d"])
+            stream.wait_event(ev[s]["d2h"])  # the slot's previous output has been read out
+            i = rot[k]
+            rot[k] = (i + 1) % len(bufs[k])
+            tb.matvec_axis1(bufs[k][i], scales[k], x_dev[s], geoms[k], o_dev[s])
+            ev[s]["kern"].record(stream)
+            with torch.cuda.stream(d2h_stream):
+                d2h_stream.wait_event(ev[s]["kern"])
+                o_host[s].copy_(o_dev[s], non_blocking=True)
+                ev[s]["d2h"].record(d2h_stream)
 
     for _ in range(args.warmup):
         e2e_step()
@@ -232,6 +253,7 @@ def run_gpu(args):
     a.record(stream)
     for _ in range(args.steps):
         e2e_step()
+    stream.wait_stream(d2h_stream)  # the timed region ends when the last output is back on the host
     b.record(stream)
     sync_all()
     e2e_ms = a.elapsed_time(b)
