@@ -34,7 +34,7 @@ def _sample(n, count, seed):
 # ------------------------------------------------------------------ expand
 
 @pytest.mark.parametrize("k", [2, 3, 4])
-@pytest.mark.parametrize("rows,cols", [(1, 256), (37, 768), (64, 2048)])
+@pytest.mark.parametrize("rows,cols", [(1, 256), (333, 256), (37, 768), (64, 2048)])
 def test_expand_bit_exact_small(oracle_mod, k, rows, cols):
     codes, scales, _ = inputs.make_linear(rows, cols, k, 1, seed_codes=11 + k, seed_scales=12)
     g = tb.Geometry(k, L, T, 1, rows, cols)
