@@ -236,6 +236,19 @@ int trellis_gemm_prefill(const uint32_t *codes, const uint16_t *scales, const ui
                          uint16_t *out, int M, const trellis_geom_t *g, trellis_stream_t stream);
 
 /*
+ * trellis_load_floor -- measurement aid with no counterpart in the pages'
+ * operations: reads an axis-1 bitstream with exactly the access pattern of
+ * trellis_matvec_axis1 (one lane per stored row, 16-byte loads of half
+ * blocks) and decodes nothing; out[r] = XOR of all words of stored row r.
+ * Its bandwidth is the HBM rate that access pattern can reach, the floor
+ * the decode-fused matvec is compared with.
+ *   codes [rows][cols*k/32] (device, 16-byte aligned)   out [rows] uint32 (device)
+ * Requires a valid axis-1 geometry without the interleaved layout.  Errors:
+ * EGEOM, EAXIS, ENULL, EALIGN, EDEVICE, ECUDA (launch).
+ */
+int trellis_load_floor(const uint32_t *codes, uint32_t *out, const trellis_geom_t *g, trellis_stream_t stream);
+
+/*
  * trellis_device_error -- diagnostic of the tensor-core kernel.  Every wait on
  * an mbarrier inside trellis_gemm_prefill is bounded (2 s); a wait that gives
  * up records a non-zero code in a device word instead of hanging the GPU.

@@ -115,6 +115,19 @@ def test_matvec_axis1_L12(oracle_mod):
     check_band(oracle_mod, bf16_bits(out), ref, ab, "axis1 L=12")
 
 
+# ------------------------------------------------------------------ load floor
+
+@pytest.mark.parametrize("k", [2, 3, 4])
+@pytest.mark.parametrize("rows,cols", [(45, 768), (17408, 5120)])
+def test_load_floor_reads_every_word(k, rows, cols):
+    """The load-only floor folds each row's words by XOR: it must have read all of them."""
+    codes, _, _ = inputs.make_linear(rows, cols, k, 1, seed_codes=61 + k)
+    g = tb.Geometry(k, L, T, 1, rows, cols)
+    got = tb.load_floor(to_dev_u32(codes), g).cpu().numpy().view(np.uint32)
+    want = np.bitwise_xor.reduce(np.ascontiguousarray(codes).view(np.uint32), axis=1)
+    assert np.array_equal(got, want)
+
+
 # ------------------------------------------------------------------ gate/up
 
 def check_gateup(oracle, gpu_bits, gref, gab, uref, uab, what):

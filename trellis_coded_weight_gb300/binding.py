@@ -28,7 +28,7 @@ STATUS_NAMES = {0: "TRELLIS_OK", -1: "TRELLIS_EGEOM", -2: "TRELLIS_EM", -3: "TRE
 EXPORTS = ("trellis_abi_version", "trellis_status_string", "trellis_check_geom", "trellis_expand_bf16",
            "trellis_matvec_axis1", "trellis_matvec_axis0", "trellis_workspace_bytes", "trellis_gateup_swiglu",
            "trellis_gemm_prefill", "trellis_device_error", "trellis_mlp_decode", "trellis_matvec_axis1_bf16w",
-           "trellis_matvec_axis0_bf16w")
+           "trellis_matvec_axis0_bf16w", "trellis_load_floor")
 
 
 class TrellisGeom(ctypes.Structure):
@@ -109,6 +109,8 @@ def load(path: str = LIB_PATH):
             lib.trellis_mlp_decode.argtypes = [vp] * 9 + [i32, g, g, vp, sz, vp]
             lib.trellis_device_error.restype = i32
             lib.trellis_device_error.argtypes = [i32]
+            lib.trellis_load_floor.restype = i32
+            lib.trellis_load_floor.argtypes = [vp, vp, g, vp]
             _lib = lib
     return _lib
 
@@ -220,6 +222,18 @@ def gemm_prefill(codes, scales, x, g: Geometry, out=None):
             _req(x, "x", (torch.bfloat16,), (M, n_in)),
             _req(out, "out", (torch.bfloat16,), (M, n_out)))
     _check("trellis_gemm_prefill", load().trellis_gemm_prefill(*args, M, ctypes.byref(g.c()), _stream(x)))
+    return out
+
+
+def load_floor(codes: torch.Tensor, g: Geometry, out: torch.Tensor = None) -> torch.Tensor:
+    """Measurement aid: read the axis-1 stream with the matvec's access pattern, decode nothing;
+    out[r] = XOR of row r's words (int32 view of uint32)."""
+    if out is None:
+        out = torch.empty(g.rows, dtype=torch.int32, device=codes.device)
+    fn = "trellis_load_floor"
+    _check(fn, load().trellis_load_floor(_req(codes, "codes", _CODES, g.codes_shape),
+                                         _req(out, "out", (torch.int32,), (g.rows,)),
+                                         ctypes.byref(g.c()), _stream(codes)))
     return out
 
 

@@ -41,6 +41,10 @@ cudaError_t launch_gemm_prefill(const uint32_t* codes, const uint16_t* scales, c
                                 uint16_t* out, int M, int k, int L, int axis, int64_t rows, int64_t cols,
                                 cudaStream_t st);
 
+// Load-only floor of the axis-1 access pattern (no decode): out[r] = XOR of row r's words.
+cudaError_t launch_load_floor(const uint32_t* codes, uint32_t* out, int k, int64_t rows, int64_t cols,
+                              cudaStream_t st);
+
 // Device error word of the tensor-core kernels (bounded waits that gave up).
 int read_device_error(int reset);
 

@@ -230,6 +230,48 @@ static cudaError_t mv1_dispatch(const Mv1Params& p, int k, int L, int M, cudaStr
   return mv1_launch_m<4, 12, GU, BW>(p, M, st);
 }
 
+// Load-only floor: the axis-1 matvec's access to the packed stream (lane =
+// row, the row's half blocks split over the CTA's warps, K 16-byte loads and
+// the spill word per half block) with no decode; each row's words are folded
+// by XOR so that the loads stay live, and the fold is stored per row.  Its
+// bandwidth is what this access pattern can reach on HBM.
+template <int K>
+__global__ void __launch_bounds__(512) load_floor_kernel(const uint32_t* codes, uint32_t* out, int64_t R, int nb) {
+  extern __shared__ uint32_t fold[];
+  constexpr int WPB = kT * K / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, S = blockDim.x >> 5;
+  const int64_t row = (int64_t)blockIdx.x * 32 + lane;
+  const int64_t rr = row < R ? row : R - 1;
+  const int c0 = (int)((int64_t)warp * 2 * nb / S), c1 = (int)((int64_t)(warp + 1) * 2 * nb / S);
+  const uint32_t* crow[1] = {codes + rr * (int64_t)nb * WPB};
+  uint32_t acc = 0;
+  for (int ci = c0; ci < c1; ++ci) {
+    HalfBlock<K, 1> hbk;
+    load_half<K, 1>(hbk, crow, ci);
+#pragma unroll
+    for (int i = 0; i <= 4 * K; ++i) acc ^= hbk.w[0][i];
+  }
+  fold[warp * 32 + lane] = acc;
+  __syncthreads();
+  if (warp != 0 || row >= R) return;
+  uint32_t v = 0;
+  for (int w = 0; w < S; ++w) v ^= fold[w * 32 + lane];
+  out[row] = v;
+}
+
+cudaError_t launch_load_floor(const uint32_t* codes, uint32_t* out, int k, int64_t rows, int64_t cols,
+                              cudaStream_t st) {
+  const int nb = (int)(cols / kT);
+  int S = 16;
+  if (S > 2 * nb) S = 2 * nb;
+  const dim3 grid((unsigned)((rows + 31) / 32)), block(32 * S);
+  const size_t sm = (size_t)S * 32 * sizeof(uint32_t);
+  if (k == 2) load_floor_kernel<2><<<grid, block, sm, st>>>(codes, out, rows, nb);
+  else if (k == 3) load_floor_kernel<3><<<grid, block, sm, st>>>(codes, out, rows, nb);
+  else load_floor_kernel<4><<<grid, block, sm, st>>>(codes, out, rows, nb);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_matvec_axis1(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
                                 uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols,
                                 cudaStream_t st) {
