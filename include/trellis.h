@@ -239,7 +239,9 @@ int trellis_gemm_prefill(const uint32_t *codes, const uint16_t *scales, const ui
  * trellis_load_floor -- measurement aid with no counterpart in the pages'
  * operations: reads an axis-1 bitstream with exactly the access pattern of
  * trellis_matvec_axis1 (one lane per stored row, 16-byte loads of half
- * blocks) and decodes nothing; out[r] = XOR of all words of stored row r.
+ * blocks) and decodes nothing; out[r] = XOR of every word it loads for
+ * stored row r: each block's words plus the spill reads of its words 4k and
+ * 0, i.e. the XOR of the row's words other than words 0 and 4k of each block.
  * Its bandwidth is the HBM rate that access pattern can reach, the floor
  * the decode-fused matvec is compared with.
  *   codes [rows][cols*k/32] (device, 16-byte aligned)   out [rows] uint32 (device)

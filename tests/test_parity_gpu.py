@@ -120,11 +120,16 @@ def test_matvec_axis1_L12(oracle_mod):
 @pytest.mark.parametrize("k", [2, 3, 4])
 @pytest.mark.parametrize("rows,cols", [(45, 768), (17408, 5120)])
 def test_load_floor_reads_every_word(k, rows, cols):
-    """The load-only floor folds each row's words by XOR: it must have read all of them."""
+    """The load-only floor folds by XOR every word it loads: all of the row's words, plus each block's
+    two spill reads (word 4K with the first half block, word 0 with the second), which cancel those
+    two words -- so the fold is the XOR of each block's words other than 0 and 4K."""
     codes, _, _ = inputs.make_linear(rows, cols, k, 1, seed_codes=61 + k)
     g = tb.Geometry(k, L, T, 1, rows, cols)
     got = tb.load_floor(to_dev_u32(codes), g).cpu().numpy().view(np.uint32)
-    want = np.bitwise_xor.reduce(np.ascontiguousarray(codes).view(np.uint32), axis=1)
+    blocks = np.ascontiguousarray(codes).view(np.uint32).reshape(rows, cols // T, T * k // 32).copy()
+    blocks[:, :, 0] = 0
+    blocks[:, :, 4 * k] = 0
+    want = np.bitwise_xor.reduce(blocks.reshape(rows, -1), axis=1)
     assert np.array_equal(got, want)
 
 

@@ -227,7 +227,7 @@ def gemm_prefill(codes, scales, x, g: Geometry, out=None):
 
 def load_floor(codes: torch.Tensor, g: Geometry, out: torch.Tensor = None) -> torch.Tensor:
     """Measurement aid: read the axis-1 stream with the matvec's access pattern, decode nothing;
-    out[r] = XOR of row r's words (int32 view of uint32)."""
+    out[r] = XOR of every word loaded for row r (int32 view of uint32)."""
     if out is None:
         out = torch.empty(g.rows, dtype=torch.int32, device=codes.device)
     fn = "trellis_load_floor"

@@ -232,7 +232,7 @@ static cudaError_t mv1_dispatch(const Mv1Params& p, int k, int L, int M, cudaStr
 
 // Load-only floor: the axis-1 matvec's access to the packed stream (lane =
 // row, the row's half blocks split over the CTA's warps, K 16-byte loads and
-// the spill word per half block) with no decode; each row's words are folded
+// the spill word per half block) with no decode; every loaded word is folded
 // by XOR so that the loads stay live, and the fold is stored per row.  Its
 // bandwidth is what this access pattern can reach on HBM.
 template <int K>
