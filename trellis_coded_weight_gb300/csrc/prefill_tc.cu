@@ -661,6 +661,10 @@ cudaError_t prefill_launch(PrefillParams p, const uint16_t* x, cudaStream_t st) 
   }
   p.nRT = (int)((p.nOut + kBM - 1) / kBM);
   p.nTiles = p.nRT * ((p.M + BN - 1) / BN);
+  // Axis 1: a decoder group's stages are C_::Groups apart within a tile; with nk a multiple of the group
+  // count they stay so across the tiles of a persistent CTA (the stage ring relies on it).  Coded widths
+  // are multiples of 256 columns, so this always holds.
+  if (AX == 1 && ((p.Kd + BK - 1) / BK) % C_::Groups != 0) return cudaErrorInvalidValue;
   const int sms = sm_count();
   // Axis 0 has few output tiles (one per 128 features): when they leave SMs idle, a cluster of S CTAs
   // splits each tile's reduction (S <= 8, the portable cluster size, and S * tiles <= SMs).
