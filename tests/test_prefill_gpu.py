@@ -40,7 +40,7 @@ def test_prefill_full_size_sampled(oracle_mod, M):
     g = tb.Geometry(k, L, T, 1, rows, cols)
     out = bf16_bits(tb.gemm_prefill(to_dev_u32(codes), to_dev_f16(scales), to_dev_bf16(x), g))
     rng = np.random.default_rng(M)
-    idx = np.unique(np.concatenate([rng.choice(rows, 24, replace=False), [0, 127, 128, rows - 1]])).astype(np.int64)
+    idx = np.unique(np.concatenate([rng.choice(rows, 24, replace=False), [0, 127, 128, 255, 256, 383, 384, rows - 1]])).astype(np.int64)
     ref, ab = oracle_mod.prefill(codes, scales, x, k, L, T, rows=idx)
     check_band(oracle_mod, out[:, idx], ref, ab, f"prefill full M={M}")
 
