@@ -33,9 +33,13 @@
 // Tile shapes: BN = 512 tokens for M > 256 (a 512-column accumulator, so each
 // decoded weight feeds 512 tokens -- decoding, not the tensor core, is the
 // costly part of this GEMM), else the smallest of 32..256 that covers M.
-// Axis 0 with fewer output tiles than SMs: a thread-block cluster of S CTAs
-// splits each tile's reduction and sums the partial accumulators through
-// distributed shared memory (epilogue, split reduction).
+// Axis 0 (stored W^T, coded along the output features): the A tile is 128
+// output features x BK stored rows; each decoder thread decodes a run of 32
+// features of one stored row (the row direction, as on axis 1) and writes each
+// weight into its feature's A row at that row's K position.  With fewer
+// output tiles than SMs, a thread-block cluster of S CTAs splits each tile's
+// reduction and sums the partial accumulators through distributed shared
+// memory (epilogue, split reduction).
 #include <cstdint>
 #include <cstring>
 #include <cuda.h>
@@ -75,22 +79,20 @@ struct PrefillParams {
 
 constexpr int kMaxChunks = 16;  // 32-column chunks of the widest accumulator (BN = 512)
 
-// CT: bytes of the per-stage code tile (axis 0 only; 0 for axis 1).
-template <int BN, int BK, int CT = 0>
+// AX0: axis-0 kernel (reserves the split reduction's chunk buffer).
+template <int BN, int BK, bool AX0 = false>
 struct Cfg {
   static constexpr int NACC = 2 * BN <= 512 ? 2 : 1;  // accumulators in tensor memory
   static constexpr int NMMA = BN > 256 ? 256 : BN;    // MMA N
   static constexpr int NH = BN / NMMA;                 // MMAs along N per 16 columns
   static constexpr int ATile = kBM * BK * 2;
   static constexpr int BTile = BN * BK * 2;
-  static constexpr int CTile = CT;
-  static constexpr int Stage = ATile + BTile + CTile;
+  static constexpr int Stage = ATile + BTile;
   static constexpr int EpiBytes = kEpiWarps * 2 * 32 * 32 * 2;  // per warp: two 32x32 bf16 sub-tiles
-  static constexpr int ScaleBytes = CT ? kDecWarps * 32 * 4 : 0;  // per-warp row scales (axis 0)
   // axis 0 split: two fp32 [32][128] chunk buffers, the first in the (then unused) bf16 epilogue staging
-  static constexpr int RedBytes = CT ? 32 * kBM * 4 : 0;
+  static constexpr int RedBytes = AX0 ? 32 * kBM * 4 : 0;
   static_assert(EpiBytes == 32 * kBM * 4, "the epilogue staging holds one fp32 chunk");
-  static constexpr int NS0 = (220 * 1024 - EpiBytes - ScaleBytes - RedBytes) / Stage;
+  static constexpr int NS0 = (220 * 1024 - EpiBytes - RedBytes) / Stage;
   static constexpr int NS = NS0 > 8 ? 8 : NS0;         // ring stages
   static constexpr int TmemCols = NACC * BN < 32 ? 32 : NACC * BN;
   static constexpr int RunsPerRow = BK / 32;            // runs of 32 positions per row and stage
@@ -99,7 +101,7 @@ struct Cfg {
   static constexpr uint32_t SBO = 8u * BK * 2u;         // bytes between 8-row groups
   static constexpr uint32_t SwMode = BK == 64 ? 2u : 4u;  // descriptor swizzle: 128B or 64B
   static constexpr CUtensorMapSwizzle TmaSw = BK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-  static constexpr size_t Smem = 1024 + (size_t)NS * Stage + EpiBytes + ScaleBytes + RedBytes + 1024;
+  static constexpr size_t Smem = 1024 + (size_t)NS * Stage + EpiBytes + RedBytes + 1024;
   static_assert(BK == 64 || BK == 32, "stage width");
   static_assert(NS >= 2, "ring too small");
   // a decoder group's consecutive stages are Groups apart: within one lap of the ring, so that an
@@ -108,11 +110,12 @@ struct Cfg {
 };
 
 // The words of one run (K words of positions 32q .. 32q+31 plus the spill
-// word, which wraps to word 0 for the block's last run) and the row scale.
+// word, which wraps to word 0 for the block's last run) and the row scale, kept
+// as its fp16 bits so that the scale's load is waited for only where it is used.
 template <int K>
 struct RunWords {
   uint32_t w[K + 1];
-  float scale;
+  uint16_t scale;
 };
 
 template <int K>
@@ -122,7 +125,7 @@ __device__ __forceinline__ void load_run(RunWords<K>& rw, const uint32_t* __rest
 #pragma unroll
   for (int i = 0; i < K; ++i) rw.w[i] = __ldg(blk + (7 - q) * K + i);
   rw.w[K] = __ldg(blk + ((8 - q) * K) % WPB);
-  rw.scale = f16_to_f32(__ldg(sc));
+  rw.scale = __ldg(sc);
 }
 
 // Decode one run into the A tile as bf16(value*scale): 16-byte chunk c of the
@@ -133,7 +136,8 @@ __device__ __forceinline__ void decode_run_to_tile(const RunWords<K>& rw, uint8_
   uint32_t s[32];
   run_states<K, L>(rw.w, s);
   const float2 nmagic = make_float2(-kMagic, -kMagic);
-  const float2 sc = make_float2(rw.scale, rw.scale);
+  const float scale = f16_to_f32(rw.scale);
+  const float2 sc = make_float2(scale, scale);
   uint32_t packed[16];
 #pragma unroll
   for (int j = 0; j < 32; j += 2) {
@@ -149,33 +153,32 @@ __device__ __forceinline__ void decode_run_to_tile(const RunWords<K>& rw, uint8_
         make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
 }
 
-// Axis 0: decode, for one output feature (a fixed position of a block, so a
-// fixed window offset), the weights of 32 consecutive stored rows from the
-// stage's code tile ct [rows][WPB words], scale each by its row's scale, and
-// write them as bf16 into the A row of that feature (K-major, swizzled).
-template <int K, int L>
-__device__ __forceinline__ void decode_col_to_tile(const uint32_t* ct, int row0, int t, const float* sc,
-                                                   uint8_t* row, int sw, int chunk0) {
-  constexpr int WPB = kT * K / 32;
-  const int o = (kT - 1 - t) * K, wi = o >> 5, sh = o & 31;
-  const int wj = (wi + 1 == WPB) ? 0 : wi + 1;
-  const uint32_t mask = (L == 32) ? 0xFFFFFFFFu : ((1u << L) - 1u);
+// Axis 0: decode one run of one stored row -- 32 consecutive output features
+// at one K position -- and write bf16(value*scale) of feature j into row j of
+// the A tile at `a` (K-major, swizzled), K position kr.  Row j's swizzle is a
+// compile-time constant because the run starts at a multiple of 32 features;
+// the 32 lanes (consecutive K positions) store into one row at once.
+template <int K, int L, int BK>
+__device__ __forceinline__ void decode_run_to_column(const RunWords<K>& rw, uint8_t* a, int kr) {
+  constexpr int RowBytes = BK * 2;
+  uint32_t s[32];
+  run_states<K, L>(rw.w, s);
   const float2 nmagic = make_float2(-kMagic, -kMagic);
-  uint32_t packed[16];
+  const float scale = f16_to_f32(rw.scale);
+  const float2 sc = make_float2(scale, scale);
+  const int kc = kr >> 3;              // 16-byte chunk of position kr in a row
+  uint8_t* base = a + (kr & 7) * 2;    // byte within the chunk
 #pragma unroll
   for (int j = 0; j < 32; j += 2) {
-    const uint32_t* w0 = ct + (row0 + j) * WPB;
-    const uint32_t* w1 = w0 + WPB;
-    const uint32_t s0 = __funnelshift_r(w0[wi], w0[wj], sh) & mask;
-    const uint32_t s1 = __funnelshift_r(w1[wi], w1[wj], sh) & mask;
-    const float2 y = __fadd2_rn(make_float2(__uint_as_float(code_magic(s0)), __uint_as_float(code_magic(s1))), nmagic);
-    const float2 wv = __fmul2_rn(value_rn2(y), make_float2(sc[j], sc[j + 1]));
-    packed[j / 2] = pack_bf16x2(wv.x, wv.y);
+    const float2 y = __fadd2_rn(make_float2(__uint_as_float(code_magic(s[j])), __uint_as_float(code_magic(s[j + 1]))),
+                                nmagic);
+    const float2 wv = __fmul2_rn(value_rn2(y), sc);
+    const uint32_t packed = pack_bf16x2(wv.x, wv.y);
+    const int swa = BK == 64 ? (j & 7) : ((j >> 1) & 3);
+    const int swb = BK == 64 ? ((j + 1) & 7) : (((j + 1) >> 1) & 3);
+    *reinterpret_cast<uint16_t*>(base + j * RowBytes + ((kc ^ swa) << 4)) = (uint16_t)(packed & 0xFFFFu);
+    *reinterpret_cast<uint16_t*>(base + (j + 1) * RowBytes + ((kc ^ swb) << 4)) = (uint16_t)(packed >> 16);
   }
-#pragma unroll
-  for (int c = 0; c < 4; ++c)
-    *reinterpret_cast<uint4*>(row + (((chunk0 + c) ^ sw) << 4)) =
-        make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
 }
 
 __device__ __forceinline__ void report(int code) { atomicCAS(&g_device_error, 0, code); }
@@ -201,8 +204,8 @@ __device__ __forceinline__ int ax1_stage_col(int ks, int nk) {
 template <int K, int L, int BN, int BK, int AX>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_out,
-                   const __grid_constant__ CUtensorMap tmap_codes, const PrefillParams p) {
-  using C_ = Cfg<BN, BK, AX == 0 ? BK * (kT * K / 32) * 4 : 0>;
+                   const PrefillParams p) {
+  using C_ = Cfg<BN, BK, AX == 0>;
   constexpr int NS = C_::NS, NACC = C_::NACC, NMMA = C_::NMMA, NH = C_::NH;
   constexpr int WPB = kT * K / 32;
   constexpr int RowBytes = BK * 2;
@@ -212,13 +215,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* a_tiles = smem;                                // NS x ATile
   uint8_t* b_tiles = smem + (size_t)NS * C_::ATile;       // NS x BTile
-  uint8_t* c_tiles = b_tiles + (size_t)NS * C_::BTile;   // NS x CTile (axis 0: code words of the stage)
   uint8_t* epi_stage = smem + (size_t)NS * C_::Stage;     // kEpiWarps x 2 x [32 tokens][32 rows] bf16
-  float* sbuf = reinterpret_cast<float*>(epi_stage + C_::EpiBytes);  // axis 0: 32 row scales per decoder warp
-  // axis 0 split: chunk buffer 0 is the epilogue staging, buffer 1 follows the row scales; [32][128] fp32 each
-  float* red[2] = {reinterpret_cast<float*>(epi_stage),
-                   reinterpret_cast<float*>(epi_stage + C_::EpiBytes + C_::ScaleBytes)};
-  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_stage + C_::EpiBytes + C_::ScaleBytes + C_::RedBytes);
+  // axis 0 split: chunk buffer 0 is the epilogue staging, buffer 1 follows it; [32][128] fp32 each
+  float* red[2] = {reinterpret_cast<float*>(epi_stage), reinterpret_cast<float*>(epi_stage + C_::EpiBytes)};
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_stage + C_::EpiBytes + C_::RedBytes);
   uint64_t* full_a = bars;                 // decoder group -> MMA
   uint64_t* full_b = bars + NS;            // TMA -> MMA (1 arrival + tx bytes)
   uint64_t* empty = bars + 2 * NS;         // MMA commit -> producer and decoders
@@ -280,10 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ks = 0; ks < kcnt; ++ks, ++g) {
           const int s = (int)(g % NS);
           if (g >= NS && !tc::mbar_wait(empty + s, (uint32_t)((g / NS) & 1) ^ 1u, kWaitNs)) { *fail = 1; break; }
-          tc::mbar_arrive_expect_tx(full_b + s, (uint32_t)(C_::BTile + C_::CTile));
-          if constexpr (AX == 0)  // the codes of this stage's stored rows, for the tile's block
-            tc::tma_load_2d(c_tiles + (size_t)s * C_::CTile, &tmap_codes, full_b + s, ((t % p.nRT) >> 1) * WPB,
-                            (kbeg + ks) * BK);
+          tc::mbar_arrive_expect_tx(full_b + s, (uint32_t)C_::BTile);
 #pragma unroll
           for (int h = 0; h < NH; ++h)
             tc::tma_load_2d(b_tiles + (size_t)s * C_::BTile + (size_t)h * NMMA * RowBytes, &tmap_x, full_b + s,
@@ -450,31 +447,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = gw >> 2;                 // which run of the stage
     const int sw = BK == 64 ? (rl & 7) : ((rl >> 1) & 3);
     if constexpr (AX == 0) {
-      // one output feature per thread (fixed window offset), 32 stored rows per run
-      float* sb = sbuf + dw * 32;
-      auto scale_of = [&](int64_t g) -> float {
-        if (g >= total) return 0.f;
-        int64_t r = (int64_t)(kbeg + g % kcnt) * BK + 32 * h + lane;
-        if (r >= p.R) r = p.R - 1;
-        return f16_to_f32(__ldg(p.scales + r));
-      };
-      float nsc = scale_of(grp);
-      for (int64_t g = grp; g < total; g += NG) {
-        const int s = (int)(g % NS);
-        const uint32_t ph = (uint32_t)((g / NS) & 1);
-        __syncwarp();
-        sb[lane] = nsc;
-        nsc = scale_of(g + NG);
-        __syncwarp();
-        if (g >= NS && !tc::mbar_wait(empty + s, ph ^ 1u, kWaitNs)) { *fail = 1; break; }
-        if (!tc::mbar_wait(full_b + s, ph, kWaitNs)) { *fail = 1; break; }  // the code tile has landed
-        const int t = cid + (int)(g / kcnt) * G;
-        const int tpos = (((t % p.nRT) * kBM) & (kT - 1)) + rl;  // position of this feature in its block
-        decode_col_to_tile<K, L>(reinterpret_cast<const uint32_t*>(c_tiles + (size_t)s * C_::CTile), 32 * h, tpos,
-                                 sb, a_tiles + (size_t)s * C_::ATile + rl * RowBytes, sw, 4 * h);
+      // Row direction: a thread owns stored row kr of the stage (K position) and run q of the tile's
+      // 128 output features; it decodes the run's 32 windows from registers and writes each weight into
+      // its feature's A row.  The run's words and the row scale are requested before the wait for the
+      // stage's ring slot, which hides their latency.
+      const int q = gw & 3;                  // run of the tile's features: 32q .. 32q+31
+      const int kr = (gw >> 2) * 32 + lane;  // stored row of the stage: 0 .. BK-1
+      const int ntot = (int)total;           // stages of this CTA (n_local * kcnt, far below 2^31)
+      int lt = grp / kcnt, ks = grp % kcnt;  // tile and stage of g, advanced incrementally
+      for (int g = grp; g < ntot; g += NG) {
+        const int s = g % NS;
+        RunWords<K> rw;
+        {
+          const int tb = (cid + lt * G) % p.nRT;  // 128-feature tile: block tb >> 1, half tb & 1
+          int64_t r = (int64_t)(kbeg + ks) * BK + kr;
+          if (r >= p.R) r = p.R - 1;  // past the reduction's end the x tile is zero
+          load_run<K>(rw, p.codes + (r * p.nb + (tb >> 1)) * WPB, 4 * (tb & 1) + q, p.scales + r);
+        }
+        if (g >= NS && !tc::mbar_wait(empty + s, (uint32_t)((g / NS) & 1) ^ 1u, kWaitNs)) { *fail = 1; break; }
+        decode_run_to_column<K, L, BK>(rw, a_tiles + (size_t)s * C_::ATile + 32 * q * RowBytes, kr);
         tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(full_a + s);
+        ks += NG;
+        while (ks >= kcnt) { ks -= kcnt; ++lt; }
       }
     } else {
       // Stage order of ax1_stage_col: a turn of this group is a half block of
@@ -493,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t nturn = (int64_t)n_local * per_tile;
       struct HalfWords {
         uint32_t w[4 * K + 1];
-        float scale;
+        uint16_t scale;  // fp16 bits, converted where used
       };
       // turn u: tile lt, half block hbk, first stage ks0 (full turns: SPH stages NG apart; tail: one stage of run r0)
       auto turn = [&](int64_t u, int& lt, int& hbk, int& ks0, int& r0) -> bool {
@@ -524,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           hw.w[4 * i] = v.x; hw.w[4 * i + 1] = v.y; hw.w[4 * i + 2] = v.z; hw.w[4 * i + 3] = v.w;
         }
         hw.w[4 * K] = __ldg(blk + (hb ? 0 : 4 * K));
-        hw.scale = f16_to_f32(__ldg(p.scales + r));
+        hw.scale = __ldg(p.scales + r);
       };
       // one stage: decode run qh (of the half block) into slot g % NS
       auto stage = [&](const RunWords<K>& rw, int64_t g) -> bool {
@@ -614,13 +610,11 @@ int sm_count() {
 
 template <int K, int L, int BN, int BK, int AX>
 cudaError_t prefill_launch(PrefillParams p, const uint16_t* x, cudaStream_t st) {
-  constexpr int WPB = kT * K / 32;
-  using C_ = Cfg<BN, BK, AX == 0 ? BK * WPB * 4 : 0>;
+  using C_ = Cfg<BN, BK, AX == 0>;
   auto fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
-  CUtensorMap map, omap, cmap;
+  CUtensorMap map, omap;
   memset(&omap, 0, sizeof(omap));
-  memset(&cmap, 0, sizeof(cmap));
   {  // x [M][Kd] bf16, boxes of [NMMA tokens][BK columns], swizzled
     const cuuint64_t dims[2] = {(cuuint64_t)p.Kd, (cuuint64_t)p.M};
     const cuuint64_t strides[1] = {(cuuint64_t)p.Kd * 2};
@@ -628,16 +622,6 @@ cudaError_t prefill_launch(PrefillParams p, const uint16_t* x, cudaStream_t st) 
     const cuuint32_t estr[2] = {1, 1};
     if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, estr,
            CU_TENSOR_MAP_INTERLEAVE_NONE, C_::TmaSw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  if (AX == 0) {  // codes [R][C*k/32] uint32, boxes of [BK stored rows][one block of words]
-    const cuuint64_t dims[2] = {(cuuint64_t)(p.C * K / 32), (cuuint64_t)p.R};
-    const cuuint64_t strides[1] = {(cuuint64_t)(p.C * K / 32) * 4};
-    const cuuint32_t box[2] = {(cuuint32_t)WPB, (cuuint32_t)BK};
-    const cuuint32_t estr[2] = {1, 1};
-    if (fn(&cmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(p.codes), dims, strides, box, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
@@ -690,11 +674,11 @@ cudaError_t prefill_launch(PrefillParams p, const uint16_t* x, cudaStream_t st) 
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, map, omap, cmap, p);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, map, omap, p);
     return e != cudaSuccess ? e : cudaGetLastError();
   }
   const int grid = p.nTiles < sms ? p.nTiles : sms;
-  kern<<<grid, kThreads, C_::Smem, st>>>(map, omap, cmap, p);
+  kern<<<grid, kThreads, C_::Smem, st>>>(map, omap, p);
   return cudaGetLastError();
 }
 
