@@ -153,31 +153,42 @@ __device__ __forceinline__ void decode_run_to_tile(const RunWords<K>& rw, uint8_
         make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
 }
 
-// Axis 0: decode one run of one stored row -- 32 consecutive output features
-// at one K position -- and write bf16(value*scale) of feature j into row j of
-// the A tile at `a` (K-major, swizzled), K position kr.  Row j's swizzle is a
-// compile-time constant because the run starts at a multiple of 32 features;
-// the 32 lanes (consecutive K positions) store into one row at once.
+// Axis 0: one warp decodes run q (32 output features) of 32 consecutive stored
+// rows (K positions 8*kc0 .. 8*kc0+31) and stores the weights transposed into
+// the K-major A tile with stmatrix .trans.  In each 8x8 block of that store,
+// lane t holds stored row t/4 and the feature pair 2(t%4), 2(t%4)+1, so lane t
+// decodes, for each of its four rows 8*kc0 + 8n + t/4, the features
+// 8i + 2(t%4) + {0,1} (i = 0..3).  Its run words are first shifted left by
+// 2(t%4)*K bits, which puts all eight windows at compile-time offsets.  Lane t
+// gives the address of A row t (feature t of the run) for K block n.
 template <int K, int L, int BK>
-__device__ __forceinline__ void decode_run_to_column(const RunWords<K>& rw, uint8_t* a, int kr) {
+__device__ __forceinline__ void decode_runs_transposed(const RunWords<K> (&rw)[4], uint8_t* a, int kc0, int lane) {
   constexpr int RowBytes = BK * 2;
-  uint32_t s[32];
-  run_states<K, L>(rw.w, s);
+  const int sh = 2 * (lane & 3) * K;  // < 32 for K <= 5
   const float2 nmagic = make_float2(-kMagic, -kMagic);
-  const float scale = f16_to_f32(rw.scale);
-  const float2 sc = make_float2(scale, scale);
-  const int kc = kr >> 3;              // 16-byte chunk of position kr in a row
-  uint8_t* base = a + (kr & 7) * 2;    // byte within the chunk
+  const int swz = BK == 64 ? (lane & 7) : ((lane >> 1) & 3);  // swizzle of A row t (runs start at multiples of 32)
+  const uint32_t row_addr = tc::smem_u32(a + lane * RowBytes);
 #pragma unroll
-  for (int j = 0; j < 32; j += 2) {
-    const float2 y = __fadd2_rn(make_float2(__uint_as_float(code_magic(s[j])), __uint_as_float(code_magic(s[j + 1]))),
-                                nmagic);
-    const float2 wv = __fmul2_rn(value_rn2(y), sc);
-    const uint32_t packed = pack_bf16x2(wv.x, wv.y);
-    const int swa = BK == 64 ? (j & 7) : ((j >> 1) & 3);
-    const int swb = BK == 64 ? ((j + 1) & 7) : (((j + 1) >> 1) & 3);
-    *reinterpret_cast<uint16_t*>(base + j * RowBytes + ((kc ^ swa) << 4)) = (uint16_t)(packed & 0xFFFFu);
-    *reinterpret_cast<uint16_t*>(base + (j + 1) * RowBytes + ((kc ^ swb) << 4)) = (uint16_t)(packed >> 16);
+  for (int n = 0; n < 4; ++n) {
+    uint32_t w[K + 1];
+    w[0] = rw[n].w[0] << sh;
+#pragma unroll
+    for (int i = 1; i <= K; ++i) w[i] = __funnelshift_l(rw[n].w[i - 1], rw[n].w[i], sh);
+    const float scale = f16_to_f32(rw[n].scale);
+    const float2 sc = make_float2(scale, scale);
+    uint32_t pk[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {  // features 8i + 2(t%4) (window at (31-8i)K after the shift) and the next
+      const uint32_t s0 = window_at<L, K + 1>(w, (31 - 8 * i) * K);
+      const uint32_t s1 = window_at<L, K + 1>(w, (30 - 8 * i) * K);
+      const float2 y = __fadd2_rn(make_float2(__uint_as_float(code_magic(s0)), __uint_as_float(code_magic(s1))), nmagic);
+      const float2 wv = __fmul2_rn(value_rn2(y), sc);
+      pk[i] = pack_bf16x2(wv.x, wv.y);
+    }
+    const uint32_t addr = row_addr + ((uint32_t)((kc0 + n) ^ swz) << 4);
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};"
+                 ::"r"(addr), "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
+                 : "memory");
   }
 }
 
@@ -447,25 +458,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = gw >> 2;                 // which run of the stage
     const int sw = BK == 64 ? (rl & 7) : ((rl >> 1) & 3);
     if constexpr (AX == 0) {
-      // Row direction: a thread owns stored row kr of the stage (K position) and run q of the tile's
-      // 128 output features; it decodes the run's 32 windows from registers and writes each weight into
-      // its feature's A row.  The run's words and the row scale are requested before the wait for the
-      // stage's ring slot, which hides their latency.
+      // Row direction: warp gw of the group takes run q of the tile's 128 output features for 32 stored
+      // rows of the stage (K positions kr0 .. kr0+31); each lane decodes two adjacent features of four of
+      // those rows, and the warp stores them transposed (decode_runs_transposed).  The run words and
+      // row scales are requested before the wait for the stage's ring slot, which hides their latency.
       const int q = gw & 3;                  // run of the tile's features: 32q .. 32q+31
-      const int kr = (gw >> 2) * 32 + lane;  // stored row of the stage: 0 .. BK-1
+      const int kr0 = (gw >> 2) * 32;        // first stored row of the warp in the stage
       const int ntot = (int)total;           // stages of this CTA (n_local * kcnt, far below 2^31)
       int lt = grp / kcnt, ks = grp % kcnt;  // tile and stage of g, advanced incrementally
       for (int g = grp; g < ntot; g += NG) {
         const int s = g % NS;
-        RunWords<K> rw;
+        RunWords<K> rw[4];
         {
           const int tb = (cid + lt * G) % p.nRT;  // 128-feature tile: block tb >> 1, half tb & 1
-          int64_t r = (int64_t)(kbeg + ks) * BK + kr;
-          if (r >= p.R) r = p.R - 1;  // past the reduction's end the x tile is zero
-          load_run<K>(rw, p.codes + (r * p.nb + (tb >> 1)) * WPB, 4 * (tb & 1) + q, p.scales + r);
+#pragma unroll
+          for (int n = 0; n < 4; ++n) {
+            int64_t r = (int64_t)(kbeg + ks) * BK + kr0 + 8 * n + (lane >> 2);
+            if (r >= p.R) r = p.R - 1;  // past the reduction's end the x tile is zero
+            load_run<K>(rw[n], p.codes + (r * p.nb + (tb >> 1)) * WPB, 4 * (tb & 1) + q, p.scales + r);
+          }
         }
-        if (g >= NS && !tc::mbar_wait(empty + s, (uint32_t)((g / NS) & 1) ^ 1u, kWaitNs)) { *fail = 1; break; }
-        decode_run_to_column<K, L, BK>(rw, a_tiles + (size_t)s * C_::ATile + 32 * q * RowBytes, kr);
+        // warp-uniform outcome: the transposing store below is a whole-warp instruction
+        if (g >= NS && !__all_sync(0xffffffffu, tc::mbar_wait(empty + s, (uint32_t)((g / NS) & 1) ^ 1u, kWaitNs))) {
+          *fail = 1;
+          break;
+        }
+        decode_runs_transposed<K, L, BK>(rw, a_tiles + (size_t)s * C_::ATile + 32 * q * RowBytes, kr0 >> 3, lane);
         tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(full_a + s);
