@@ -504,15 +504,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int F = nk / SPH / NG, full = F * NG * SPH;
       const int tail = nk - full > grp ? (nk - full - grp + NG - 1) / NG : 0;  // this group's stages past the rounds
       const int per_tile = F + tail;
-      const int64_t nturn = (int64_t)n_local * per_tile;
+      const int nturn = n_local * per_tile;  // turns of this group (a few thousand at most)
       struct HalfWords {
         uint32_t w[4 * K + 1];
         uint16_t scale;  // fp16 bits, converted where used
       };
-      // turn u: tile lt, half block hbk, first stage ks0 (full turns: SPH stages NG apart; tail: one stage of run r0)
-      auto turn = [&](int64_t u, int& lt, int& hbk, int& ks0, int& r0) -> bool {
-        lt = (int)(u / per_tile);
-        const int v = (int)(u % per_tile);
+      // A turn cursor (tile lt, turn v of the tile), advanced without division.
+      struct Cursor {
+        int lt, v;
+      };
+      auto advance = [&](Cursor& c) {
+        if (++c.v == per_tile) { c.v = 0; ++c.lt; }
+      };
+      // turn v of a tile: half block hbk and first stage ks0 (full turns: SPH stages NG apart; tail: one
+      // stage of run r0)
+      auto turn = [&](int v, int& hbk, int& ks0, int& r0) -> bool {
         if (v < F) {
           hbk = v * NG + grp; ks0 = v * NG * SPH + grp; r0 = -1;
           return true;
@@ -521,11 +527,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         hbk = F * NG + (ks0 - full) / SPH; r0 = (ks0 - full) % SPH;
         return false;
       };
-      auto fetch = [&](HalfWords& hw, int64_t u) {
-        if (u >= nturn) return;
-        int lt, hbk, ks0, r0;
-        turn(u, lt, hbk, ks0, r0);
-        const int t = cid + lt * G;
+      auto fetch = [&](HalfWords& hw, const Cursor& c) {
+        if (c.lt >= n_local || c.v >= per_tile) return;  // past the last turn (or a group without turns)
+        int hbk, ks0, r0;
+        turn(c.v, hbk, ks0, r0);
+        const int t = cid + c.lt * G;
         int64_t r = (int64_t)(t % p.nRT) * kBM + rl;
         if (r >= p.R) r = p.R - 1;  // rows past the end decode row R-1 and are never stored
         const int c0 = hbk * 128;   // first column of the half block
@@ -541,8 +547,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         hw.scale = __ldg(p.scales + r);
       };
       // one stage: decode run qh (of the half block) into slot g % NS
-      auto stage = [&](const RunWords<K>& rw, int64_t g) -> bool {
-        const int s = (int)(g % NS);
+      auto stage = [&](const RunWords<K>& rw, int g) -> bool {
+        const int s = g % NS;
         if (g >= NS && !tc::mbar_wait(empty + s, (uint32_t)((g / NS) & 1) ^ 1u, kWaitNs)) return false;
         decode_run_to_tile<K, L>(rw, a_tiles + (size_t)s * C_::ATile + rl * RowBytes, sw, 4 * h);
         tc::fence_proxy_async_smem();
@@ -550,10 +556,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) tc::mbar_arrive(full_a + s);
         return true;
       };
-      auto process = [&](const HalfWords& hw, int64_t u) -> bool {
-        int lt, hbk, ks0, r0;
-        const bool round = turn(u, lt, hbk, ks0, r0);
-        const int64_t gbase = (int64_t)lt * nk + ks0;
+      auto process = [&](const HalfWords& hw, const Cursor& c) -> bool {
+        int hbk, ks0, r0;
+        const bool round = turn(c.v, hbk, ks0, r0);
+        const int gbase = c.lt * nk + ks0;  // this CTA's stage index
         if (round) {
 #pragma unroll
           for (int ss = 0; ss < SPH; ++ss) {  // run qh = ss*RPR + h, at words (3-qh)*K
@@ -564,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               else rw.w[i] = hw.w[(3 - ss) * K + i];
             }
             rw.scale = hw.scale;
-            if (!stage(rw, gbase + (int64_t)ss * NG)) return false;
+            if (!stage(rw, gbase + ss * NG)) return false;
           }
           return true;
         }
@@ -582,16 +588,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         rw.scale = hw.scale;
         return stage(rw, gbase);
       };
+      // two turns in flight: the words of turn u + 2 load while turn u decodes
       HalfWords ha, hb2;
-      int64_t u = 0;
-      fetch(ha, 0);
-      fetch(hb2, 1);
-      while (u < nturn) {
-        if (!process(ha, u)) { *fail = 1; break; }
-        fetch(ha, u + 2);
+      Cursor cu{0, 0}, cf{0, 0};  // the turn being decoded, the turn being fetched
+      fetch(ha, cf);
+      advance(cf);
+      fetch(hb2, cf);
+      advance(cf);
+      for (int u = 0; u < nturn;) {
+        if (!process(ha, cu)) { *fail = 1; break; }
+        advance(cu);
+        fetch(ha, cf);
+        advance(cf);
         if (++u >= nturn) break;
-        if (!process(hb2, u)) { *fail = 1; break; }
-        fetch(hb2, u + 2);
+        if (!process(hb2, cu)) { *fail = 1; break; }
+        advance(cu);
+        fetch(hb2, cf);
+        advance(cf);
         ++u;
       }
     }
