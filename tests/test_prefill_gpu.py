@@ -87,8 +87,10 @@ def test_prefill_axis0_split_is_deterministic():
         assert torch.equal(tb.gemm_prefill(dc, ds, dx, g).view(torch.int16), first.view(torch.int16))
 
 
-@pytest.mark.parametrize("M", [64, 512])
+@pytest.mark.parametrize("M", [64, 512, 2048])
 def test_prefill_axis0_full_size_sampled(oracle_mod, M):
+    # M=2048: 160 tiles on the SMs run as a full unsplit wave plus the leftover tiles with split
+    # reductions (features 4096.. of the last token tile); the sampled columns reach into both.
     rows, cols, k = 17408, 5120, 3
     codes, scales, x = inputs.make_linear(rows, cols, k, M, sigma=0.5, x_len=rows)
     g = tb.Geometry(k, L, T, 0, rows, cols)

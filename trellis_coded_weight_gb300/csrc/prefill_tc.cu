@@ -75,6 +75,7 @@ struct PrefillParams {
   int nRT, nTiles;  // output-feature tiles, total tiles
   int tma_out;      // 1: out written by TMA tensor stores (nOut % 8 == 0)
   int S;            // axis 0: CTAs (a cluster) splitting each tile's reduction; 1 = no split
+  int t0;           // first tile of this launch: it runs tiles t0 .. t0 + nTiles - 1
 };
 
 constexpr int kMaxChunks = 16;  // 32-column chunks of the widest accumulator (BN = 512)
@@ -286,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int64_t g = 0, issued = 0;
       for (int lt = 0; lt < n_local && !*fail; ++lt) {
-        const int t = cid + lt * G;
+        const int t = p.t0 + cid + lt * G;
         const int m0 = (t / p.nRT) * BN;
         for (int ks = 0; ks < kcnt; ++ks, ++g) {
           const int s = (int)(g % NS);
@@ -345,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // barriers are single-use; no CTA leaves before the owners of its last
     // two chunks are done with its buffers.
     const int sp = warp & 3;
-    const int t = cid;
+    const int t = p.t0 + cid;
     const int64_t rbase = (int64_t)(t % p.nRT) * kBM + 32 * sp;
     const int64_t row = rbase + lane;
     const int m0 = (t / p.nRT) * BN;
@@ -403,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(acc_full + buf, (uint32_t)(use & 1), kWaitNs));
       tc::fence_after_sync();
       if (!ok) { *fail = 1; break; }
-      const int t = cid + lt * G;
+      const int t = p.t0 + cid + lt * G;
       const int64_t rbase = (int64_t)(t % p.nRT) * kBM + 32 * sp;  // first row of this warp's 32
       const int64_t row = rbase + lane;
       const int m0 = (t / p.nRT) * BN;
@@ -470,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = g % NS;
         RunWords<K> rw[4];
         {
-          const int tb = (cid + lt * G) % p.nRT;  // 128-feature tile: block tb >> 1, half tb & 1
+          const int tb = (p.t0 + cid + lt * G) % p.nRT;  // 128-feature tile: block tb >> 1, half tb & 1
 #pragma unroll
           for (int n = 0; n < 4; ++n) {
             int64_t r = (int64_t)(kbeg + ks) * BK + kr0 + 8 * n + (lane >> 2);
@@ -531,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (c.lt >= n_local || c.v >= per_tile) return;  // past the last turn (or a group without turns)
         int hbk, ks0, r0;
         turn(c.v, hbk, ks0, r0);
-        const int t = cid + c.lt * G;
+        const int t = p.t0 + cid + c.lt * G;
         int64_t r = (int64_t)(t % p.nRT) * kBM + rl;
         if (r >= p.R) r = p.R - 1;  // rows past the end decode row R-1 and are never stored
         const int c0 = hbk * 128;   // first column of the half block
@@ -681,36 +682,50 @@ cudaError_t prefill_launch(PrefillParams p, const uint16_t* x, cudaStream_t st) 
   // are multiples of 256 columns, so this always holds.
   if (AX == 1 && ((p.Kd + BK - 1) / BK) % C_::Groups != 0) return cudaErrorInvalidValue;
   const int sms = sm_count();
-  // Axis 0 has few output tiles (one per 128 features): when they leave SMs idle, a cluster of S CTAs
-  // splits each tile's reduction (S <= 8, the portable cluster size, and S * tiles <= SMs).
-  int S = 1;
-  if (AX == 0) {
-    S = sms / p.nTiles;
+  const int nk = (int)((p.Kd + BK - 1) / BK);
+  // one launch over tiles [t0, t0 + count): persistent CTAs (S = 1) or one tile per cluster of S CTAs
+  auto launch_part = [&](int t0, int count, int S) -> cudaError_t {
+    PrefillParams q = p;
+    q.t0 = t0;
+    q.nTiles = count;
+    q.S = S;
+    if (S > 1) {
+      cudaLaunchConfig_t cfg{};
+      cfg.gridDim = dim3((unsigned)(count * S));
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = C_::Smem;
+      cfg.stream = st;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = (unsigned)S;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, map, omap, q);
+      return e != cudaSuccess ? e : cudaGetLastError();
+    }
+    const int grid = count < sms ? count : sms;
+    kern<<<grid, kThreads, C_::Smem, st>>>(map, omap, q);
+    return cudaGetLastError();
+  };
+  // Axis 0 has few output tiles (one per 128 features), each with a long reduction.  When they leave SMs
+  // idle, a cluster of S CTAs splits each tile's reduction (S <= 8, the portable cluster size, and S *
+  // tiles <= SMs).  When they overrun whole waves, the full waves run unsplit and the tiles left over run
+  // in a second launch with their reductions split, instead of as a nearly empty wave.
+  auto split_of = [&](int count) {
+    int S = sms / count;
     if (S > 8) S = 8;
-    const int nk = (int)((p.Kd + BK - 1) / BK);
     if (S > nk) S = nk;
-    if (S < 1) S = 1;
+    return S < 1 ? 1 : S;
+  };
+  if (AX == 0 && p.nTiles > sms && p.nTiles % sms != 0) {
+    const int rem = p.nTiles % sms, main = p.nTiles - rem;
+    const cudaError_t e = launch_part(0, main, 1);
+    if (e != cudaSuccess) return e;
+    return launch_part(main, rem, split_of(rem));
   }
-  p.S = S;
-  if (S > 1) {
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)(p.nTiles * S));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = C_::Smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)S;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, map, omap, p);
-    return e != cudaSuccess ? e : cudaGetLastError();
-  }
-  const int grid = p.nTiles < sms ? p.nTiles : sms;
-  kern<<<grid, kThreads, C_::Smem, st>>>(map, omap, p);
-  return cudaGetLastError();
+  return launch_part(0, p.nTiles, AX == 0 ? split_of(p.nTiles) : 1);
 }
 
 template <int K, int L, int AX>
