@@ -1,5 +1,6 @@
-// prefill_tc.cu -- prefill GEMM over an axis-1 trellis matrix on the 5th-
-// generation tensor cores (tcgen05), any M >= 1 (intended for M > 4).
+// prefill_tc.cu -- prefill GEMM over a trellis matrix (axis 1, and the
+// stored-transposed axis 0) on the 5th-generation tensor cores (tcgen05),
+// any M >= 1 (intended for M > 4).
 //
 // What is computed ("trellis-tiled-prefill.ts" diff page: tiledTrellisPrefill;
 // "trellis-linear.ts": the expand + matmul path of TrellisLinear.forward):
@@ -33,13 +34,15 @@
 // Tile shapes: BN = 512 tokens for M > 256 (a 512-column accumulator, so each
 // decoded weight feeds 512 tokens -- decoding, not the tensor core, is the
 // costly part of this GEMM), else the smallest of 32..256 that covers M.
-// Axis 0 (stored W^T, coded along the output features): the A tile is 128
-// output features x BK stored rows; each decoder thread decodes a run of 32
-// features of one stored row (the row direction, as on axis 1) and writes each
-// weight into its feature's A row at that row's K position.  With fewer
-// output tiles than SMs, a thread-block cluster of S CTAs splits each tile's
-// reduction and sums the partial accumulators through distributed shared
-// memory (epilogue, split reduction).
+// Axis 0 (stored W^T, coded along the output features;
+// "trellis-splitk-prefill.ts" diff page): the A tile is 128 output features
+// x BK stored rows.  A decoder warp decodes a run of 32 features along each of
+// 32 stored rows (the coding direction) and stores the weights transposed
+// into the K-major A tile with stmatrix .trans (decode_runs_transposed).
+// With fewer output tiles than SMs, a thread-block cluster of S CTAs splits
+// each tile's reduction and sums the partial accumulators through
+// distributed shared memory (epilogue, split reduction); with more, the full
+// waves run unsplit and the leftover tiles run split in a second launch.
 #include <cstdint>
 #include <cstring>
 #include <cuda.h>
