@@ -716,9 +716,13 @@ cudaError_t prefill_launch(PrefillParams p, const uint16_t* x, cudaStream_t st) 
   // idle, a cluster of S CTAs splits each tile's reduction (S <= 8, the portable cluster size, and S *
   // tiles <= SMs).  When they overrun whole waves, the full waves run unsplit and the tiles left over run
   // in a second launch with their reductions split, instead of as a nearly empty wave.
+  // The split reduction runs BN/32 chunk rounds whose cost grows with S (measured at BN = 512: about
+  // 20 us per CTA of the cluster against 300 us for a whole tile), so S stops at round(sqrt(240 / chunks)):
+  // 4 for BN = 512, 5 for BN = 256, 8 below.
+  constexpr int kSplitCap = BN >= 512 ? 4 : (BN >= 256 ? 5 : 8);
   auto split_of = [&](int count) {
     int S = sms / count;
-    if (S > 8) S = 8;
+    if (S > kSplitCap) S = kSplitCap;
     if (S > nk) S = nk;
     return S < 1 ? 1 : S;
   };
