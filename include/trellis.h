@@ -217,9 +217,10 @@ int trellis_mlp_decode(const uint32_t *gcodes, const uint16_t *gscales, const ui
                        size_t workspace_bytes, trellis_stream_t stream);
 
 /*
- * trellis_gemm_prefill -- prefill GEMM over an axis-1 matrix for any M >= 1
- * (intended for M > 4) ("trellis-tiled-prefill.ts": tiledTrellisPrefill and
- * the expand + matmul path of TrellisLinear.forward).  Weight tiles are
+ * trellis_gemm_prefill -- prefill GEMM over an axis-1 or axis-0 matrix for any
+ * M >= 1 (intended for M > 4) ("trellis-tiled-prefill.ts": tiledTrellisPrefill
+ * and the expand + matmul path of TrellisLinear.forward;
+ * "trellis-splitk-prefill.ts" for axis 0).  Weight tiles are
  * decoded into shared memory as bf16 (the expand numerics: bf16 of the
  * correctly rounded value times the scale), x tiles arrive by TMA, and the
  * 5th-generation tensor cores (tcgen05, accumulators in tensor memory)
@@ -228,8 +229,11 @@ int trellis_mlp_decode(const uint32_t *gcodes, const uint16_t *gscales, const ui
  * accumulated in fp32.
  *   codes [rows][cols*k/32]   scales [rows]   x [M][cols] bf16   out [M][rows] bf16
  * Axis 0 (stored W^T, the down projection): out[m][c] = bf16( sum_r e(r,c) *
- * x[m][r] ), x [M][rows], out [M][cols]; the decoded tile is built from the
- * stage's code rows staged by TMA, one output feature per decoder thread.
+ * x[m][r] ), x [M][rows], out [M][cols]; weights are decoded along the stored
+ * rows and stored transposed into the tile, and the long reduction over rows
+ * is split across thread-block clusters where tiles alone would leave SMs
+ * idle (possibly as a second launch on `stream` for the tiles left after
+ * whole waves).  Results are deterministic: repeated calls give equal bits.
  * Requires M >= 1, no interleaved layout, and for axis 0 rows % 8 == 0.
  */
 int trellis_gemm_prefill(const uint32_t *codes, const uint16_t *scales, const uint16_t *x,
