@@ -98,3 +98,18 @@ def test_prefill_axis0_full_size_sampled(oracle_mod, M):
     idx = np.unique(np.r_[np.arange(0, cols, 331), 127, 128, 255, 256, cols - 1]).astype(np.int64)
     ref, ab = oracle_mod.matvec_axis0_bf16w(codes, scales, x, k, L, T, cols=idx)
     check_band(oracle_mod, out[:, idx], ref, ab, f"prefill axis0 full M={M}")
+
+
+def test_prefill_axis0_leftover_tiles_short_reduction(oracle_mod):
+    # 42 feature tiles x 4 token tiles (the last one ragged: 1600 = 3*512 + 64) = 168 tiles: a full unsplit
+    # wave, then the leftover tiles split over clusters whose size the 3-stage reduction caps.
+    rows, cols, M, k = 96, 5376, 1600, 3
+    codes, scales, x = inputs.make_linear(rows, cols, k, M, seed_codes=141, seed_x=142, sigma=0.5, x_len=rows)
+    g = tb.Geometry(k, L, T, 0, rows, cols)
+    dc, ds, dx = to_dev_u32(codes), to_dev_f16(scales), to_dev_bf16(x)
+    out = tb.gemm_prefill(dc, ds, dx, g)
+    assert torch.equal(tb.gemm_prefill(dc, ds, dx, g).view(torch.int16), out.view(torch.int16))
+    assert tb.device_error(reset=True) == 0
+    idx = np.unique(np.r_[np.arange(0, cols, 97), 127, 128, 5247, 5248, cols - 1]).astype(np.int64)
+    ref, ab = oracle_mod.matvec_axis0_bf16w(codes, scales, x, k, L, T, cols=idx)
+    check_band(oracle_mod, bf16_bits(out)[:, idx], ref, ab, f"prefill axis0 leftover M={M} {rows}x{cols}")
