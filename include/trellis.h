@@ -255,6 +255,22 @@ int trellis_gemm_prefill(const uint32_t *codes, const uint16_t *scales, const ui
 int trellis_load_floor(const uint32_t *codes, uint32_t *out, const trellis_geom_t *g, trellis_stream_t stream);
 
 /*
+ * trellis_prefill_plan -- the tile plan trellis_gemm_prefill follows for
+ * (M, g) on a GPU with `sms` SMs (sms < 1: the current device's).  Host
+ * arithmetic only: no CUDA call unless sms < 1, nothing launched.  Writes
+ * the tokens per tile to *tokens_per_tile and, per launch, three ints to
+ * launches[3*i ..]: first tile, tile count, and CTAs per tile (a thread-
+ * block cluster splitting each tile's reduction when > 1).  Tiles are 128
+ * output features x tokens_per_tile tokens; tile t is feature tile
+ * t % ceil(features/128), token tile t / ceil(features/128).
+ *   launches: caller-owned, room for 2 launches (6 ints).
+ * Returns the number of launches (1 or 2), or a negative status: the
+ * geometry and M checks of trellis_gemm_prefill, ENULL, or EDEVICE when
+ * sms < 1 and no usable device is current.
+ */
+int trellis_prefill_plan(int M, const trellis_geom_t *g, int sms, int *tokens_per_tile, int *launches);
+
+/*
  * trellis_device_error -- diagnostic of the tensor-core kernel.  Every wait on
  * an mbarrier inside trellis_gemm_prefill is bounded (2 s); a wait that gives
  * up records a non-zero code in a device word instead of hanging the GPU.

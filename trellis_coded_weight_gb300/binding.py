@@ -28,7 +28,7 @@ STATUS_NAMES = {0: "TRELLIS_OK", -1: "TRELLIS_EGEOM", -2: "TRELLIS_EM", -3: "TRE
 EXPORTS = ("trellis_abi_version", "trellis_status_string", "trellis_check_geom", "trellis_expand_bf16",
            "trellis_matvec_axis1", "trellis_matvec_axis0", "trellis_workspace_bytes", "trellis_gateup_swiglu",
            "trellis_gemm_prefill", "trellis_device_error", "trellis_mlp_decode", "trellis_matvec_axis1_bf16w",
-           "trellis_matvec_axis0_bf16w", "trellis_load_floor")
+           "trellis_matvec_axis0_bf16w", "trellis_load_floor", "trellis_prefill_plan")
 
 
 class TrellisGeom(ctypes.Structure):
@@ -111,6 +111,8 @@ def load(path: str = LIB_PATH):
             lib.trellis_device_error.argtypes = [i32]
             lib.trellis_load_floor.restype = i32
             lib.trellis_load_floor.argtypes = [vp, vp, g, vp]
+            lib.trellis_prefill_plan.restype = i32
+            lib.trellis_prefill_plan.argtypes = [i32, g, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
             _lib = lib
     return _lib
 
@@ -235,6 +237,16 @@ def load_floor(codes: torch.Tensor, g: Geometry, out: torch.Tensor = None) -> to
                                          _req(out, "out", (torch.int32,), (g.rows,)),
                                          ctypes.byref(g.c()), _stream(codes)))
     return out
+
+
+def prefill_plan(M: int, g: Geometry, sms: int = 0):
+    """The tile plan of gemm_prefill (host arithmetic): (tokens per tile, [(first tile, tiles, CTAs per
+    tile), ...]).  sms < 1 takes the current device's SM count."""
+    bn = ctypes.c_int32(0)
+    buf = (ctypes.c_int32 * 6)()
+    n = load().trellis_prefill_plan(M, ctypes.byref(g.c()), sms, ctypes.byref(bn), buf)
+    _check("trellis_prefill_plan", n if n < 0 else 0)
+    return bn.value, [tuple(buf[3 * i:3 * i + 3]) for i in range(n)]
 
 
 def device_error(reset: bool = False) -> int:

@@ -217,6 +217,28 @@ int trellis_gemm_prefill(const uint32_t* codes, const uint16_t* scales, const ui
                                                   static_cast<cudaStream_t>(stream)));
 }
 
+int trellis_prefill_plan(int M, const trellis_geom_t* g, int sms, int* tokens_per_tile, int* launches) {
+  int st = geom_ok(g);
+  if (st) return st;
+  if (g->interleave) return TRELLIS_EGEOM;
+  if (g->axis == 0 && g->rows % 8 != 0) return TRELLIS_EGEOM;
+  if (M < 1 || M > (1 << 24)) return TRELLIS_EM;
+  if (!tokens_per_tile || !launches) return TRELLIS_ENULL;
+  if (sms < 1) {  // the current device's SM count
+    if ((st = device_ok())) return st;
+    sms = trellis::device_sm_count();
+  }
+  trellis::PrefillLaunch plan[2];
+  const int n = trellis::prefill_plan(M, g->axis, g->axis == 1 ? g->rows : g->cols, g->axis == 1 ? g->cols : g->rows,
+                                      sms, tokens_per_tile, plan);
+  for (int i = 0; i < n; ++i) {
+    launches[3 * i] = plan[i].t0;
+    launches[3 * i + 1] = plan[i].count;
+    launches[3 * i + 2] = plan[i].S;
+  }
+  return n;
+}
+
 int trellis_load_floor(const uint32_t* codes, uint32_t* out, const trellis_geom_t* g, trellis_stream_t stream) {
   int st = trellis_check_geom(g);
   if (st) return st;

@@ -41,6 +41,17 @@ cudaError_t launch_gemm_prefill(const uint32_t* codes, const uint16_t* scales, c
                                 uint16_t* out, int M, int k, int L, int axis, int64_t rows, int64_t cols,
                                 cudaStream_t st);
 
+// Tile plan of the prefill GEMM (host arithmetic only): tokens per tile and up
+// to two launches over the output tiles, each [t0, t0 + count) with S CTAs per
+// tile (S > 1: a cluster splitting the tile's reduction).  Returns the number
+// of launches.
+struct PrefillLaunch {
+  int t0, count, S;
+};
+int prefill_plan(int M, int axis, int64_t nOut, int64_t Kd, int sms, int* tokens_per_tile, PrefillLaunch* launches);
+// SM count of the current device (148 if it cannot be read).
+int device_sm_count();
+
 // Load-only floor of the axis-1 access pattern (no decode): out[r] = XOR of row r's words.
 cudaError_t launch_load_floor(const uint32_t* codes, uint32_t* out, int k, int64_t rows, int64_t cols,
                               cudaStream_t st);

@@ -644,7 +644,8 @@ int sm_count() {
 }
 
 template <int K, int L, int BN, int BK, int AX>
-cudaError_t prefill_launch(PrefillParams p, const uint16_t* x, cudaStream_t st) {
+cudaError_t prefill_launch(PrefillParams p, const uint16_t* x, cudaStream_t st, const PrefillLaunch* plan,
+                           int nplan) {
   using C_ = Cfg<BN, BK, AX == 0>;
   auto fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
@@ -685,7 +686,6 @@ cudaError_t prefill_launch(PrefillParams p, const uint16_t* x, cudaStream_t st) 
   // are multiples of 256 columns, so this always holds.
   if (AX == 1 && ((p.Kd + BK - 1) / BK) % C_::Groups != 0) return cudaErrorInvalidValue;
   const int sms = sm_count();
-  const int nk = (int)((p.Kd + BK - 1) / BK);
   // one launch over tiles [t0, t0 + count): persistent CTAs (S = 1) or one tile per cluster of S CTAs
   auto launch_part = [&](int t0, int count, int S) -> cudaError_t {
     PrefillParams q = p;
@@ -712,51 +712,74 @@ cudaError_t prefill_launch(PrefillParams p, const uint16_t* x, cudaStream_t st) 
     kern<<<grid, kThreads, C_::Smem, st>>>(map, omap, q);
     return cudaGetLastError();
   };
-  // Axis 0 has few output tiles (one per 128 features), each with a long reduction.  When they leave SMs
-  // idle, a cluster of S CTAs splits each tile's reduction (S <= 8, the portable cluster size, and S *
-  // tiles <= SMs).  When they overrun whole waves, the full waves run unsplit and the tiles left over run
-  // in a second launch with their reductions split, instead of as a nearly empty wave.
-  // The split reduction runs BN/32 chunk rounds whose cost grows with S (measured at BN = 512: about
-  // 20 us per CTA of the cluster against 300 us for a whole tile), so S stops at round(sqrt(240 / chunks)):
-  // 4 for BN = 512, 5 for BN = 256, 8 below.
-  constexpr int kSplitCap = BN >= 512 ? 4 : (BN >= 256 ? 5 : 8);
-  auto split_of = [&](int count) {
-    int S = sms / count;
-    if (S > kSplitCap) S = kSplitCap;
-    if (S > nk) S = nk;
-    return S < 1 ? 1 : S;
-  };
-  if (AX == 0 && p.nTiles > sms && p.nTiles % sms != 0) {
-    const int rem = p.nTiles % sms, main = p.nTiles - rem;
-    const cudaError_t e = launch_part(0, main, 1);
+  for (int i = 0; i < nplan; ++i) {
+    const cudaError_t e = launch_part(plan[i].t0, plan[i].count, plan[i].S);
     if (e != cudaSuccess) return e;
-    return launch_part(main, rem, split_of(rem));
   }
-  return launch_part(0, p.nTiles, AX == 0 ? split_of(p.nTiles) : 1);
+  return cudaSuccess;
 }
 
 template <int K, int L, int AX>
-cudaError_t prefill_bn(const PrefillParams& p, const uint16_t* x, cudaStream_t st) {
-  if (p.M <= 32) return prefill_launch<K, L, 32, 64, AX>(p, x, st);
-  if (p.M <= 64) return prefill_launch<K, L, 64, 64, AX>(p, x, st);
-  if (p.M <= 128) return prefill_launch<K, L, 128, 64, AX>(p, x, st);
-  if (p.M <= 256) return prefill_launch<K, L, 256, 64, AX>(p, x, st);
-  return prefill_launch<K, L, 512, 32, AX>(p, x, st);
+cudaError_t prefill_bn(const PrefillParams& p, const uint16_t* x, cudaStream_t st, int BN, const PrefillLaunch* plan,
+                       int nplan) {
+  if (BN == 32) return prefill_launch<K, L, 32, 64, AX>(p, x, st, plan, nplan);
+  if (BN == 64) return prefill_launch<K, L, 64, 64, AX>(p, x, st, plan, nplan);
+  if (BN == 128) return prefill_launch<K, L, 128, 64, AX>(p, x, st, plan, nplan);
+  if (BN == 256) return prefill_launch<K, L, 256, 64, AX>(p, x, st, plan, nplan);
+  return prefill_launch<K, L, 512, 32, AX>(p, x, st, plan, nplan);
 }
 
 template <int AX>
 cudaError_t prefill_axis(const PrefillParams& p, const uint16_t* x, int k, int L, cudaStream_t st) {
+  PrefillLaunch plan[2];
+  int BN = 0;
+  const int nplan = prefill_plan(p.M, AX, p.nOut, p.Kd, sm_count(), &BN, plan);
   if (L == 16) {
-    if (k == 2) return prefill_bn<2, 16, AX>(p, x, st);
-    if (k == 3) return prefill_bn<3, 16, AX>(p, x, st);
-    return prefill_bn<4, 16, AX>(p, x, st);
+    if (k == 2) return prefill_bn<2, 16, AX>(p, x, st, BN, plan, nplan);
+    if (k == 3) return prefill_bn<3, 16, AX>(p, x, st, BN, plan, nplan);
+    return prefill_bn<4, 16, AX>(p, x, st, BN, plan, nplan);
   }
-  if (k == 2) return prefill_bn<2, 12, AX>(p, x, st);
-  if (k == 3) return prefill_bn<3, 12, AX>(p, x, st);
-  return prefill_bn<4, 12, AX>(p, x, st);
+  if (k == 2) return prefill_bn<2, 12, AX>(p, x, st, BN, plan, nplan);
+  if (k == 3) return prefill_bn<3, 12, AX>(p, x, st, BN, plan, nplan);
+  return prefill_bn<4, 12, AX>(p, x, st, BN, plan, nplan);
 }
 
 }  // namespace
+
+// Tiles: 128 output features x BN tokens, BN = 512 for M > 256 (stages of 32 columns), else the smallest
+// of 32..256 covering M (stages of 64 columns).  Axis 1 runs one persistent launch.  Axis 0 has few
+// output tiles (one per 128 features), each with a long reduction:
+//   - when they leave SMs idle, a cluster of S CTAs splits each tile's reduction (S * tiles <= SMs);
+//   - when they overrun whole waves, the full waves run unsplit and the tiles left over run split in a
+//     second launch, instead of as a nearly empty wave.
+// The split reduction runs BN/32 chunk rounds whose cost grows with S (measured at BN = 512: about 20 us
+// per CTA of the cluster against 300 us for a whole tile), so S stops at round(sqrt(240 / chunks)): 4 for
+// BN = 512, 5 for BN = 256, 8 (the portable cluster size) below; and at the reduction's stage count.
+int device_sm_count() { return sm_count(); }
+
+int prefill_plan(int M, int axis, int64_t nOut, int64_t Kd, int sms, int* tokens_per_tile, PrefillLaunch* launches) {
+  const int BN = M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : M <= 256 ? 256 : 512;
+  const int BK = BN == 512 ? 32 : 64;
+  const int nk = (int)((Kd + BK - 1) / BK);
+  const int nTiles = (int)((nOut + kBM - 1) / kBM) * ((M + BN - 1) / BN);
+  const int cap = BN >= 512 ? 4 : (BN >= 256 ? 5 : 8);
+  if (sms < 1) sms = 1;
+  auto split_of = [&](int count) {
+    int S = sms / count;
+    if (S > cap) S = cap;
+    if (S > nk) S = nk;
+    return S < 1 ? 1 : S;
+  };
+  *tokens_per_tile = BN;
+  if (axis == 0 && nTiles > sms && nTiles % sms != 0) {
+    const int rem = nTiles % sms;
+    launches[0] = PrefillLaunch{0, nTiles - rem, 1};
+    launches[1] = PrefillLaunch{nTiles - rem, rem, split_of(rem)};
+    return 2;
+  }
+  launches[0] = PrefillLaunch{0, nTiles, axis == 0 ? split_of(nTiles) : 1};
+  return 1;
+}
 
 cudaError_t launch_gemm_prefill(const uint32_t* codes, const uint16_t* scales, const uint16_t* x, uint16_t* out,
                                 int M, int k, int L, int axis, int64_t rows, int64_t cols, cudaStream_t st) {
