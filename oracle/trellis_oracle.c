@@ -6,10 +6,9 @@
  * CPU-baseline leg may load this library.  The product path (the CUDA library
  * and its Python binding) never calls it and shares no code with it.
  *
- * Source: the "mlx-bun 0.2.0 -> 0.4.0" diff pages of trellis-linear.ts
- * (page 55, the file's header comment "TrellisLinear -- a linear layer over
- * PACKED trellis-coded weights" and its kernel sources) and of
- * trellis-tiled-prefill.ts / trellis-vector-expand.ts (page 56).
+ * Source: the "mlx-bun 0.2.0 -> 0.4.0" diff pages of trellis-linear.ts (the
+ * file's header comment on the packed linear layer, and its kernel sources)
+ * and of trellis-tiled-prefill.ts / trellis-vector-expand.ts.
  *
  * What is computed, in the pages' order:
  *   format   .weight is a uint32 bitstream [rows, cols*k/32], .scales is fp16
