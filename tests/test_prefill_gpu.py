@@ -113,3 +113,27 @@ def test_prefill_axis0_leftover_tiles_short_reduction(oracle_mod):
     idx = np.unique(np.r_[np.arange(0, cols, 97), 127, 128, 5247, 5248, cols - 1]).astype(np.int64)
     ref, ab = oracle_mod.matvec_axis0_bf16w(codes, scales, x, k, L, T, cols=idx)
     check_band(oracle_mod, bf16_bits(out)[:, idx], ref, ab, f"prefill axis0 leftover M={M} {rows}x{cols}")
+
+
+def test_prefill_axis0_L12_split(oracle_mod):
+    # L = 12 through the axis-0 decoder (4 tiles, each reduction split over 4 CTAs)
+    rows, cols, M, k = 256, 512, 40, 3
+    codes, scales, x = inputs.make_linear(rows, cols, k, M, seed_codes=151, seed_x=152, sigma=0.5, x_len=rows)
+    g = tb.Geometry(k, 12, T, 0, rows, cols)
+    out = tb.gemm_prefill(to_dev_u32(codes), to_dev_f16(scales), to_dev_bf16(x), g)
+    assert tb.device_error(reset=True) == 0
+    ref, ab = oracle_mod.matvec_axis0_bf16w(codes, scales, x, k, 12, T)
+    check_band(oracle_mod, bf16_bits(out), ref, ab, "prefill axis0 L=12")
+
+
+def test_prefill_axis0_leftover_tiles_one_stage(oracle_mod):
+    # a 32-row reduction is a single stage: the leftover tiles run unsplit, as a second persistent launch
+    # that starts at a tile offset
+    rows, cols, M, k = 32, 5376, 1600, 2
+    codes, scales, x = inputs.make_linear(rows, cols, k, M, seed_codes=161, seed_x=162, sigma=0.5, x_len=rows)
+    g = tb.Geometry(k, L, T, 0, rows, cols)
+    out = tb.gemm_prefill(to_dev_u32(codes), to_dev_f16(scales), to_dev_bf16(x), g)
+    assert tb.device_error(reset=True) == 0
+    idx = np.unique(np.r_[np.arange(0, cols, 89), 127, 128, 5247, 5248, cols - 1]).astype(np.int64)
+    ref, ab = oracle_mod.matvec_axis0_bf16w(codes, scales, x, k, L, T, cols=idx)
+    check_band(oracle_mod, bf16_bits(out)[:, idx], ref, ab, f"prefill axis0 one-stage leftover M={M}")
