@@ -96,11 +96,19 @@ float or_code_val(int y) {
   return num / den;
 }
 
-/* Table of y and value for every state s < 2^L (L <= 24). */
+/* Table of y and value for every state s < 2^L (L <= 24), built by a second
+ * route that shares nothing with or_code_y: x is walked through the states
+ * by repeated addition of a in 32-bit unsigned arithmetic (x(0) = b,
+ * x(s+1) = x(s) + a, wrapping mod 2^32), and the byte sum is the "two
+ * byte-pair adds" form of the HEADER source's trellis_y: add the even bytes
+ * to the odd bytes as two 16-bit lanes, then add the two lanes.  Tests
+ * compare this table with or_code_y over every state. */
 void or_lut(int L, int32_t *ytab, float *vtab) {
   const uint32_t n = 1u << L;
-  for (uint32_t s = 0; s < n; ++s) {
-    const int y = or_code_y(s);
+  uint32_t x = OR_B;
+  for (uint32_t s = 0; s < n; ++s, x += OR_A) {
+    const uint32_t pairs = (x & 0x00FF00FFu) + ((x >> 8) & 0x00FF00FFu); /* two lanes, each <= 510 */
+    const int y = (int)((pairs & 0xFFFFu) + (pairs >> 16)) - 510;
     if (ytab) ytab[s] = y;
     if (vtab) vtab[s] = or_code_val(y);
   }

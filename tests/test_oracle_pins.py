@@ -60,14 +60,45 @@ def test_decode_targets_each_byte(oracle_mod, x, y):
     assert oracle_mod.code_y(s) == y
 
 
-def test_decode_range_and_values_all_L16_states(oracle_mod):
-    """y stays in [-510, 510] for every state (byte sums lie in [0, 1020])."""
-    ys, vs = oracle_mod.lut(16)
+@pytest.mark.parametrize("L", [12, 16])
+def test_decode_range_and_independent_table_all_states(oracle_mod, L):
+    """Every state of a 2^L table: y stays in [-510, 510] (byte sums lie in
+    [0, 1020]), and the table -- built by walking x = b + s*a incrementally and
+    summing bytes with the two byte-pair adds of trellis_y (HEADER source) --
+    equals the per-state decode (multiply, then bytes by division and
+    remainder) at all 2^L states."""
+    ys, vs = oracle_mod.lut(L)
+    assert ys.size == 1 << L
     assert ys.min() >= -510 and ys.max() <= 510
-    # the independently built table agrees with per-state decoding
-    for s in (0, 1, 2, 255, 256, 4095, 65535, 12345, 54321):
-        assert ys[s] == oracle_mod.code_y(s)
-        assert vs[s] == oracle_mod.code_val(int(ys[s]))
+    per_state = np.array([oracle_mod.code_y(s) for s in range(1 << L)], dtype=np.int32)
+    assert np.array_equal(ys, per_state)
+    # the table's values are the correctly rounded y/d of its own y
+    vals = {y: oracle_mod.code_val(y) for y in np.unique(ys).tolist()}
+    assert np.array_equal(vs, np.array([vals[int(y)] for y in ys], dtype=np.float32))
+
+
+def _numpy_y(L):
+    """A third formulation for the regression values: numpy uint64 products,
+    bytes by shifts, vectorised over all 2^L states."""
+    s = np.arange(1 << L, dtype=np.uint64)
+    x = (s * np.uint64(A) + np.uint64(B)) % np.uint64(1 << 32)
+    return sum(((x >> np.uint64(8 * i)) & np.uint64(255)).astype(np.int64) for i in range(4)) - 510
+
+
+@pytest.mark.parametrize("L,lo,hi,distinct", [(16, -483, 469, 908), (12, -448, 454, 713)])
+def test_decode_regression_values(oracle_mod, L, lo, hi, distinct):
+    """Regression values of the code over all 2^L states, derived when the
+    method was surveyed and re-derived independently since: the range of y,
+    the number of distinct y, and at L = 16 mean(y) = -0.0582 and
+    var(y/d) = 1.00018 (the code is built to have unit variance; d is the
+    fp32 rounding of sqrt(21845), the standard deviation of a sum of four
+    uniform bytes)."""
+    ys, vs = oracle_mod.lut(L)
+    assert (int(ys.min()), int(ys.max()), int(np.unique(ys).size)) == (lo, hi, distinct)
+    assert np.array_equal(ys, _numpy_y(L))
+    if L == 16:
+        assert abs(float(ys.mean()) - (-0.0582275390625)) < 1e-12
+        assert abs(float(np.var(vs.astype(np.float64))) - 1.00018) < 5e-6
 
 
 def test_decode_statistics_over_the_full_state_space(oracle_mod):
