@@ -34,3 +34,24 @@ def oracle_mod():
     import oracle
     oracle.build()
     return oracle
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Per parity check: outputs compared, how many sit more than one bf16 ulp
+    from bf16(ref) (allowed only where the fp32 band is wider than an ulp),
+    and the largest distance."""
+    try:
+        from util import BAND_STATS
+    except Exception:
+        return
+    if not BAND_STATS:
+        return
+    tr = terminalreporter
+    tr.section("bf16 distance from bf16(ref) per parity check")
+    total = sum(n for _, n, _, _ in BAND_STATS)
+    over = sum(o for _, _, o, _ in BAND_STATS)
+    worst = max(m for _, _, _, m in BAND_STATS)
+    tr.write_line(f"{len(BAND_STATS)} checks, {total} outputs, {over} more than 1 ulp away, largest {worst} ulp")
+    for what, n, o, m in BAND_STATS:
+        if o or m > 1:
+            tr.write_line(f"  {what}: {o} of {n} outputs more than 1 ulp away, largest {m} ulp")

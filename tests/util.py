@@ -22,6 +22,11 @@ from trellis_coded_weight_gb300 import inputs
 REL_TOL = 1e-5
 ABS_TOL = 1e-6
 
+# One entry per check_band call: (what, outputs, outputs more than one bf16
+# ulp from bf16(ref), largest distance in ulps).  The session's terminal
+# summary prints them (tests/conftest.py).
+BAND_STATS: list = []
+
 
 def to_dev_u32(a: np.ndarray, dev="cuda") -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int32)).to(dev)
@@ -74,4 +79,5 @@ def check_band(oracle, gpu_bits: np.ndarray, ref: np.ndarray, absum: np.ndarray,
     ulps = np.abs(g - mid)
     allowed = np.maximum(1, np.maximum(hi - mid, mid - lo))
     assert np.all(ulps <= allowed), f"{what}: output farther from bf16(ref) than the band allows"
-    return int(ulps.max())
+    BAND_STATS.append((what, int(ulps.size), int((ulps > 1).sum()), int(ulps.max()) if ulps.size else 0))
+    return int(ulps.max()) if ulps.size else 0
