@@ -164,11 +164,14 @@ size_t trellis_workspace_bytes(int M, const trellis_geom_t *g);
  * the library defines; every GPU that loads the library holds that array
  * until the process exits.  The call allocates nothing: it clears the
  * array's arrival counters with cudaMemsetAsync on `stream` and launches the
- * axis-0 kernel.  The first call on a device looks up the array's device
- * address (cudaGetSymbolAddress, with that device current) and caches it;
- * make that first call before any stream capture.  All calls share the one
- * array, so calls whose executions overlap on the GPU race: issue them on
- * one stream or otherwise serialise them.
+ * axis-0 kernel.  Each call looks up the array's device address
+ * (cudaGetSymbolAddress, with the caller's device current) and keeps it per
+ * device; a call whose stream is being captured into a CUDA graph uses the
+ * kept address, so make the first call on each device before any stream
+ * capture (a capture-time call with no kept address returns TRELLIS_ECUDA).
+ * The fresh lookup keeps ordinary calls valid after cudaDeviceReset.  All
+ * calls share the one array, so calls whose executions overlap on the GPU
+ * race: issue them on one stream or otherwise serialise them.
  *
  * Arguments, shapes and results are those of trellis_matvec_axis0.  Returns
  * TRELLIS_EWORKSPACE when trellis_workspace_bytes(M, g) exceeds

@@ -126,6 +126,12 @@ def _stream(t: torch.Tensor) -> int:
     return torch.cuda.current_stream(t.device).cuda_stream
 
 
+def _on(t: torch.Tensor):
+    """Make the tensor's device current for the C call: the library reads the
+    current device (its SM count, kernel attributes) and launches on it."""
+    return torch.cuda.device(t.device)
+
+
 def _req(t: torch.Tensor, name: str, dtypes, shape):
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
@@ -148,7 +154,8 @@ def expand_bf16(codes, scales, g: Geometry, out=None):
     args = (_req(codes, "codes", _CODES, g.codes_shape),
             _req(scales, "scales", (torch.float16,), (g.rows,)),
             _req(out, "out", (torch.bfloat16,), (g.rows, g.cols)))
-    _check("trellis_expand_bf16", load().trellis_expand_bf16(*args, ctypes.byref(g.c()), _stream(codes)))
+    with _on(codes):
+        _check("trellis_expand_bf16", load().trellis_expand_bf16(*args, ctypes.byref(g.c()), _stream(codes)))
     return out
 
 
@@ -164,7 +171,8 @@ def matvec_axis1(codes, scales, x, g: Geometry, out=None, bf16_weights: bool = F
             _req(x, "x", (torch.bfloat16,), (M, g.cols)),
             _req(out, "out", (torch.bfloat16,), (M, g.rows)))
     fn = "trellis_matvec_axis1_bf16w" if bf16_weights else "trellis_matvec_axis1"
-    _check(fn, getattr(load(), fn)(*args, M, ctypes.byref(g.c()), _stream(x)))
+    with _on(x):
+        _check(fn, getattr(load(), fn)(*args, M, ctypes.byref(g.c()), _stream(x)))
     return out
 
 
@@ -195,7 +203,8 @@ def matvec_axis0(codes, scales, x, g: Geometry, workspace, out=None, bf16_weight
             _req(out, "out", (torch.bfloat16,), (M, g.cols)))
     nbytes = workspace.numel() * workspace.element_size()
     fn = "trellis_matvec_axis0_bf16w" if bf16_weights else "trellis_matvec_axis0"
-    _check(fn, getattr(load(), fn)(*args, M, ctypes.byref(g.c()), workspace.data_ptr(), nbytes, _stream(x)))
+    with _on(x):
+        _check(fn, getattr(load(), fn)(*args, M, ctypes.byref(g.c()), workspace.data_ptr(), nbytes, _stream(x)))
     return out
 
 
@@ -208,7 +217,8 @@ def gateup_swiglu(gcodes, gscales, ucodes, uscales, x, g: Geometry, out=None):
     args = (_req(gcodes, "gcodes", _CODES, shp), _req(gscales, "gscales", (torch.float16,), (g.rows,)),
             _req(ucodes, "ucodes", _CODES, shp), _req(uscales, "uscales", (torch.float16,), (g.rows,)),
             _req(x, "x", (torch.bfloat16,), (M, g.cols)), _req(out, "out", (torch.bfloat16,), (M, g.rows)))
-    _check("trellis_gateup_swiglu", load().trellis_gateup_swiglu(*args, M, ctypes.byref(g.c()), _stream(x)))
+    with _on(x):
+        _check("trellis_gateup_swiglu", load().trellis_gateup_swiglu(*args, M, ctypes.byref(g.c()), _stream(x)))
     return out
 
 
@@ -223,7 +233,8 @@ def gemm_prefill(codes, scales, x, g: Geometry, out=None):
             _req(scales, "scales", (torch.float16,), (g.rows,)),
             _req(x, "x", (torch.bfloat16,), (M, n_in)),
             _req(out, "out", (torch.bfloat16,), (M, n_out)))
-    _check("trellis_gemm_prefill", load().trellis_gemm_prefill(*args, M, ctypes.byref(g.c()), _stream(x)))
+    with _on(x):
+        _check("trellis_gemm_prefill", load().trellis_gemm_prefill(*args, M, ctypes.byref(g.c()), _stream(x)))
     return out
 
 
@@ -232,10 +243,9 @@ def load_floor(codes: torch.Tensor, g: Geometry, out: torch.Tensor = None) -> to
     out[r] = XOR of every word loaded for row r (int32 view of uint32)."""
     if out is None:
         out = torch.empty(g.rows, dtype=torch.int32, device=codes.device)
-    fn = "trellis_load_floor"
-    _check(fn, load().trellis_load_floor(_req(codes, "codes", _CODES, g.codes_shape),
-                                         _req(out, "out", (torch.int32,), (g.rows,)),
-                                         ctypes.byref(g.c()), _stream(codes)))
+    args = (_req(codes, "codes", _CODES, g.codes_shape), _req(out, "out", (torch.int32,), (g.rows,)))
+    with _on(codes):
+        _check("trellis_load_floor", load().trellis_load_floor(*args, ctypes.byref(g.c()), _stream(codes)))
     return out
 
 
@@ -271,8 +281,10 @@ def mlp_decode(gcodes, gscales, ucodes, uscales, dcodes, dscales, x, g_up: Geome
     if not workspace.is_cuda or not workspace.is_contiguous():
         raise ValueError("workspace must be a contiguous CUDA tensor")
     nbytes = workspace.numel() * workspace.element_size()
-    _check("trellis_mlp_decode", load().trellis_mlp_decode(*args, M, ctypes.byref(g_up.c()), ctypes.byref(g_down.c()),
-                                                          workspace.data_ptr(), nbytes, _stream(x)))
+    with _on(x):
+        _check("trellis_mlp_decode", load().trellis_mlp_decode(*args, M, ctypes.byref(g_up.c()),
+                                                              ctypes.byref(g_down.c()), workspace.data_ptr(), nbytes,
+                                                              _stream(x)))
     return hidden, out
 
 

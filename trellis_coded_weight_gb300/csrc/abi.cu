@@ -10,15 +10,13 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "devcache.h"
 #include "launch.h"
 #include "trellis.h"
 
 namespace {
 
 constexpr int kAbiVersion = 101;
-constexpr int kMaxDevices = 64;
-// 0 = unknown, 1 = usable sm_103 device, -1 = not usable
-int g_device_ok[kMaxDevices];
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -47,14 +45,16 @@ int device_ok() {
     cudaGetLastError();
     return TRELLIS_EDEVICE;
   }
-  if (dev < kMaxDevices && g_device_ok[dev] != 0) return g_device_ok[dev] > 0 ? TRELLIS_OK : TRELLIS_EDEVICE;
-  int major = 0, minor = 0;
-  const bool ok = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
-                  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
-                  major == 10 && minor == 3;
-  if (!ok) cudaGetLastError();
-  if (dev < kMaxDevices) g_device_ok[dev] = ok ? 1 : -1;
-  return ok ? TRELLIS_OK : TRELLIS_EDEVICE;
+  static trellis::PerDevice<int> ok_of;
+  const auto probe = [dev] {
+    int major = 0, minor = 0;
+    const bool ok = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+                    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
+                    major == 10 && minor == 3;
+    if (!ok) cudaGetLastError();
+    return ok ? TRELLIS_OK : TRELLIS_EDEVICE;
+  };
+  return dev < trellis::kMaxDevices ? ok_of.get(dev, probe, TRELLIS_EDEVICE) : probe();
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? TRELLIS_OK : TRELLIS_ECUDA; }

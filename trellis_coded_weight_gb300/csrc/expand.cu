@@ -21,6 +21,7 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "devcache.h"
 #include "launch.h"
 
 namespace trellis {
@@ -128,14 +129,18 @@ template <int K, int L>
 static cudaError_t expand_launch(const uint32_t* codes, const uint16_t* scales, uint16_t* out, int64_t rows, int nb,
                                 int interleave, cudaStream_t st) {
   // one wave: as many CTAs as fit on every SM at once, each warp one item range
-  static int per_sm = 0;
-  if (!per_sm) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, expand_kernel<K, L>, kExpandThreads, 0) != cudaSuccess ||
-        per_sm < 1)
-      per_sm = 1;
-  }
-  int dev = 0, sms = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  static PerDevice<int> per_sm_of;  // per instantiation and device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
+  const int per_sm = per_sm_of.get(dev, [] {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, expand_kernel<K, L>, kExpandThreads, 0) != cudaSuccess) {
+      cudaGetLastError();
+      n = 1;
+    }
+    return n < 1 ? 1 : n;
+  }, 1);
+  const int sms = device_sm_count();
   const int64_t items = rows * nb;
   int64_t nblk = (items + 2 * (kExpandThreads / 32) - 1) / (2 * (kExpandThreads / 32));  // >= two items per warp
   if (nblk > (int64_t)sms * per_sm) nblk = (int64_t)sms * per_sm;

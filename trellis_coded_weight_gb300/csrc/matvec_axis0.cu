@@ -30,10 +30,10 @@
 //     that cover it) folds the partials in CTA order, stores bf16 and resets
 //     the counter -- one launch, deterministic, no atomics on data.
 #include <cstdint>
-#include <mutex>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "devcache.h"
 #include "launch.h"
 
 namespace trellis {
@@ -309,31 +309,19 @@ __global__ void __launch_bounds__(32 * ax0_warps<M>(), 1) ax0_kernel(const Ax0Pa
   }
 }
 
-int ax0_sm_count() {
-  static std::mutex mu;
-  static int cached[64];
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!cached[dev]) {
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    cached[dev] = n;
-  }
-  return cached[dev];
-}
-
 template <int K, int L, int M, bool BW, bool IL>
 static cudaError_t ax0_launch1(const Ax0Params& p, cudaStream_t st) {
   constexpr int W = ax0_warps<M>();
   const size_t smem = ((((size_t)p.stage * M + 3) & ~(size_t)3) + (size_t)W * M * kT + (BW ? (size_t)p.stage : 0)) *
                       sizeof(float);
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
+  static PerDevice<cudaError_t> attr_of;  // function attributes are per device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
+  const cudaError_t attr_err = attr_of.get(dev, [] {
     const size_t most = ((kAx0StageRows * M + 3) & ~(size_t)3) * sizeof(float) + (size_t)W * M * kT * sizeof(float) +
                         (BW ? kAx0StageRows * sizeof(float) : 0);
-    attr_err = cudaFuncSetAttribute(ax0_kernel<K, L, M, BW, IL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
-  });
+    return cudaFuncSetAttribute(ax0_kernel<K, L, M, BW, IL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
+  }, cudaErrorInvalidDevice);
   if (attr_err != cudaSuccess) return attr_err;
   ax0_kernel<K, L, M, BW, IL><<<p.G, 32 * W, smem, st>>>(p);
   return cudaGetLastError();
@@ -367,7 +355,7 @@ static cudaError_t ax0_dispatch(const uint32_t* codes, const uint16_t* scales, c
   p.counter = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) +
                                           (size_t)(kAx0MaxCtas + p.nb) * (size_t)M * kT * sizeof(float));
   p.R = rows; p.C = cols; p.N = (int64_t)p.nb * rows;
-  int64_t G = ax0_sm_count();
+  int64_t G = device_sm_count();
   if (G > kAx0MaxCtas) G = kAx0MaxCtas;
   if (G > (p.N + kAx0MinRows - 1) / kAx0MinRows) G = (p.N + kAx0MinRows - 1) / kAx0MinRows;
   if (G < 1) G = 1;

@@ -29,6 +29,7 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "devcache.h"
 #include "launch.h"
 
 namespace trellis {
@@ -194,12 +195,17 @@ static int mv1_splits(int nb, int regs) {
 
 template <int K, int L, int M, bool GU, bool BW>
 static cudaError_t mv1_launch(const Mv1Params& p, cudaStream_t st) {
-  static int regs = 0;  // per instantiation
-  if (!regs) {
+  static PerDevice<int> regs_of;  // per instantiation and device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
+  const int regs = regs_of.get(dev, [] {
     cudaFuncAttributes a;
-    if (cudaFuncGetAttributes(&a, mv1_kernel<K, L, M, GU, BW>) != cudaSuccess) return cudaGetLastError();
-    regs = a.numRegs;
-  }
+    if (cudaFuncGetAttributes(&a, mv1_kernel<K, L, M, GU, BW>) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;  // mv1_splits assumes 64 registers
+    }
+    return a.numRegs;
+  }, 0);
   const int S = mv1_splits(p.nb, regs);
   const int nmat = GU ? 2 : 1;
   const size_t sm = (size_t)S * M * (kT / 2) * sizeof(float) + (size_t)nmat * S * M * 32 * sizeof(float);

@@ -12,12 +12,16 @@
 //
 // The array is a file-scope __device__ object of kNoAllocScratchBytes bytes.
 // Every GPU that loads the library holds it until the process exits.  Host
-// code cannot use the array's name as a device address, so the first call on
-// each device looks the address up with cudaGetSymbolAddress (with that
-// device current) and caches it; that first call should come before any
-// stream capture.  All calls share the one array: the arrival counters are
-// cleared on the caller's stream before every launch, and calls whose
-// executions overlap on the GPU race on the shared partial sums.
+// code cannot use the array's name as a device address: each call looks the
+// address up with cudaGetSymbolAddress (with the caller's device current) and
+// keeps it per device.  A call made while its stream is being captured into a
+// CUDA graph uses the kept address instead of looking it up, so the first call
+// on each device should come before any stream capture.  Looking the address
+// up again on ordinary calls keeps it valid after cudaDeviceReset, which
+// reloads the module and may move the array.  All calls share the one array:
+// the arrival counters are cleared on the caller's stream before every
+// launch, and calls whose executions overlap on the GPU race on the shared
+// partial sums.
 #include <cstdint>
 #include <mutex>
 #include <cuda_runtime.h>
@@ -36,16 +40,21 @@ void* g_scratch_ptr[kMaxDev];
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Device address of the scratch array on the current device (set up once per
-// device), or nullptr on a CUDA error.
-void* scratch_for_current_device() {
+// Device address of the scratch array on the current device, or nullptr on a
+// CUDA error (or during capture before any ordinary call on this device).
+void* scratch_for_current_device(cudaStream_t s) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
     cudaGetLastError();
     return nullptr;
   }
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
   std::lock_guard<std::mutex> lock(g_setup_mu);
-  if (!g_scratch_ptr[dev]) {
+  if (cap == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
       cudaGetLastError();
@@ -78,12 +87,12 @@ extern "C" int trellis_matvec_axis0_noalloc(const uint32_t* codes, const uint16_
     cudaGetLastError();
     return TRELLIS_EDEVICE;
   }
-  void* ws = scratch_for_current_device();
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* ws = scratch_for_current_device(s);
   if (!ws) return TRELLIS_ECUDA;
 
   // The arrival counters follow the partial sums; they must start at zero.
   const size_t counters = need - (((size_t)(g->cols / g->T) * sizeof(uint32_t) + 15) & ~(size_t)15);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(static_cast<char*>(ws) + counters, 0, need - counters, s) != cudaSuccess) return TRELLIS_ECUDA;
   const cudaError_t e =
       trellis::launch_matvec_axis0(codes, scales, x, out, M, g->k, g->L, g->rows, g->cols, g->interleave, ws, s);

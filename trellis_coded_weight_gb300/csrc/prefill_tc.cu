@@ -50,6 +50,7 @@
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
+#include "devcache.h"
 #include "launch.h"
 #include "tc_ptx.cuh"
 
@@ -637,10 +638,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 int sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+  static PerDevice<int> sms_of;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
     return 148;
-  return n;
+  }
+  return sms_of.get(dev, [dev] {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      n = 148;
+    }
+    return n;
+  }, 148);
 }
 
 template <int K, int L, int BN, int BK, int AX>
@@ -673,12 +684,13 @@ cudaError_t prefill_launch(PrefillParams p, const uint16_t* x, cudaStream_t st, 
       p.tma_out = 1;
   }
   auto kern = prefill_kernel<K, L, BN, BK, AX>;
-  static bool attr_set = false;  // per instantiation
-  if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_::Smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static PerDevice<cudaError_t> attr_of;  // per instantiation; function attributes are per device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
+  const cudaError_t attr_err = attr_of.get(dev, [kern] {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_::Smem);
+  }, cudaErrorInvalidDevice);
+  if (attr_err != cudaSuccess) return attr_err;
   p.nRT = (int)((p.nOut + kBM - 1) / kBM);
   p.nTiles = p.nRT * ((p.M + BN - 1) / BN);
   // Axis 1: a decoder group's stages are C_::Groups apart within a tile; with nk a multiple of the group
