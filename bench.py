@@ -1,18 +1,27 @@
 #!/usr/bin/env python3
 """Benchmark of the trellis-coded linear layers on GB300.
 
-Workload (one step): the axis-1 decode-fused matvec at the MLP up-projection
+Headline (one step): the axis-1 decode-fused matvec at the MLP up-projection
 shape R=17408 out rows x C=5120 in cols, L=16, T=256, for every k in {2,3,4}
 and every M in {1,2,3,4} -- twelve launches over packed weights.  `value` is
 the packed-weight bytes of those twelve launches divided by the step time
-(GB/s); the prefill GEMM (R=17408, C=5120, k=2, M=2048) is timed in the same
-run and reported as TFLOP/s under "prefill".
+(GB/s), timed over exactly --steps steps.
+
+The same run times every other row of the hot path at its full size, each in
+`breakdown` with its median and p10/p90 launch time, its algorithmic bytes or
+FLOPs and its fraction of the measured peak: the fused gate/up SwiGLU layer
+(two 17408 x 5120 matrices, k = 2, 3), the axis-0 down projection (stored
+W^T 17408 x 5120, k = 2, 3), the bf16 expansion (k = 2..4), the tensor-core
+prefill GEMM (k = 2, M = 32 / 512 / 2048, next to expand + cuBLAS), the axis-0
+prefill (k = 3, M = 8 / 64 / 512 / 2048, next to expand + cuBLAS), the decode
+MLP block as a CUDA graph, and two load-only floors of the packed stream.
 
 Inputs are seeded and synthetic (uniform random code words, fp16 scales
-U[0.005, 0.02], bf16 x ~ N(0,1)).  Code buffers rotate through a set larger
-than twice the L2 cache, so every launch streams its weights from HBM.
+U[0.005, 0.02], bf16 x ~ N(0,1), or N(0, 0.5) for the axis-0 input).  Code
+buffers rotate through a set larger than twice the L2 cache, so every launch
+streams its weights from HBM.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--extra]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Under torchrun every rank runs the same per-GPU workload (weak scaling); the
 reported time is the maximum over ranks and `value` sums all ranks' bytes.
@@ -38,7 +47,8 @@ sys.path.insert(0, ROOT)
 METRIC = "packed-weight HBM GB/s (frac of GB300 peak) at M=1..4; prefill TFLOP/s at M=2048"
 R, C, L, T = 17408, 5120, 16, 256
 KS, MS = (2, 3, 4), (1, 2, 3, 4)
-PREFILL_M = 2048
+PREFILL_M = (32, 512, 2048)
+PREFILL0_M = (8, 64, 512, 2048)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -62,13 +72,16 @@ def workload_desc():
 
 
 class ClockSampler:
-    """Samples nvidia-smi clocks and throttle reasons while running."""
+    """Samples nvidia-smi clocks and throttle reasons while running; every
+    sample carries its host time, so a window (the timed region) can be
+    summarised on its own."""
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, index: int):
-        self.index, self.proc, self.lines = index, None, []
+        self.index, self.proc, self.samples = index, None, []
 
     def __enter__(self):
         try:
@@ -77,13 +90,22 @@ class ClockSampler:
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.th = threading.Thread(target=self._read, daemon=True)
             self.th.start()
+            time.sleep(0.3)  # the first sample arrives before the measured work starts
         except Exception:
             self.proc = None
         return self
 
     def _read(self):
         for ln in self.proc.stdout:
-            self.lines.append(ln.strip())
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm, mx = float(parts[0]), float(parts[1])
+            except ValueError:
+                continue
+            reasons = {nm for nm, v in zip(self.NAMES, parts[3:7]) if v.lower() == "active"}
+            self.samples.append((time.time(), sm, mx, reasons))
 
     def __exit__(self, *a):
         if self.proc:
@@ -93,25 +115,12 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self):
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 7:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
-            except ValueError:
-                continue
-            for nm, v in zip(names, parts[3:7]):
-                if v.lower() == "active":
-                    reasons.add(nm)
-        if not sm:
+    def summary(self, window=None):
+        s = self.samples if window is None else [x for x in self.samples if window[0] <= x[0] <= window[1]]
+        if not s:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return {"sm_mhz": statistics.median(x[1] for x in s), "sm_max_mhz": max(x[2] for x in s),
+                "reasons": sorted(set().union(*(x[3] for x in s))), "samples": len(s)}
 
 
 def dist_env():
@@ -136,6 +145,38 @@ def _dev_bf16(a, dev):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
 
 
+class Timer:
+    """Launch timing on the launching stream with CUDA events: a batch of n launches bracketed by two events
+    (the mean), and per-launch event pairs (p10/p90).  A short device sleep ahead of each batch lets the host
+    queue the launches, so no host gaps fall inside it."""
+
+    def __init__(self, torch, dev, stream, n):
+        self.torch, self.dev, self.stream, self.n = torch, dev, stream, n
+
+    def __call__(self, fn, nrot=1):
+        torch = self.torch
+        for i in range(3):
+            fn(i % nrot)
+        torch.cuda.synchronize(self.dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(int(5e6))
+        a.record(self.stream)
+        for i in range(self.n):
+            fn(i % nrot)
+        b.record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        mean_ms = a.elapsed_time(b) / self.n
+        es = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(self.n)]
+        torch.cuda._sleep(int(5e6))
+        for i in range(self.n):
+            es[i][0].record(self.stream)
+            fn(i % nrot)
+            es[i][1].record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        ts = sorted(x.elapsed_time(y) for x, y in es)
+        return {"us": mean_ms * 1e3, "us_p10_p90": [ts[int(0.1 * (len(ts) - 1))] * 1e3, ts[int(0.9 * (len(ts) - 1))] * 1e3]}
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as tdist
@@ -158,7 +199,7 @@ def run_gpu(args):
     stream = torch.cuda.current_stream(dev)
     l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 132 << 20))
 
-    # ---- inputs: rotating code sets (larger than 2x L2 per k), scales, x ----
+    # ---- inputs of the headline: rotating code sets (larger than 2x L2 per k), scales, x ----
     bufs, scales, geoms = {}, {}, {}
     for k in KS:
         nrot = int(2 * l2 // packed_bytes(k)) + 2
@@ -189,52 +230,53 @@ def run_gpu(args):
         if world > 1:
             tdist.barrier()
 
-    for _ in range(args.warmup):
-        step()
-    # ---- timed region: exactly K steps, per-launch events on the launch stream ----
-    ev = {(k, M): [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-          for k in KS for M in MS}
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sync_all()
+    res = {"world": world, "rank": rank}
     with ClockSampler(local) as clk:
+        for _ in range(args.warmup):
+            step()
+        # ---- timed region: exactly K steps, per-launch events on the launch stream ----
+        ev = {(k, M): [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+              for k in KS for M in MS}
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        sync_all()
+        h0 = time.time()
         t0.record(stream)
         for s in range(args.steps):
             step({key: ev[key][s] for key in ev})
         t1.record(stream)
         sync_all()
-    ms_total = t0.elapsed_time(t1)
+        h1 = time.time()
+        ms_total = t0.elapsed_time(t1)
+        if world > 1:
+            tt = torch.tensor([ms_total], device=dev, dtype=torch.float64)
+            tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
+            ms_total = float(tt.item())
+        per_launch, spread = {}, {}
+        for key in ev:
+            ts = sorted(e[0].elapsed_time(e[1]) for e in ev[key])
+            per_launch[key] = sum(ts) / len(ts)
+            spread[key] = (ts[int(0.1 * (len(ts) - 1))], ts[int(0.9 * (len(ts) - 1))])
+        step_bytes = sum(packed_bytes(k) for k in KS for M in MS)
+        res.update(value=world * step_bytes * args.steps / (ms_total * 1e-3) / 1e9, ms_total=ms_total,
+                   per_launch=per_launch, spread=spread, launches=len(KS) * len(MS) * args.steps,
+                   timed_window=(h0, h1))
+        res["e2e"] = run_e2e(args, torch, tdist, tb, dev, stream, bufs, scales, geoms, xs, rot, world, sync_all)
+        if rank == 0 or args.all_rows:
+            timer = Timer(torch, dev, stream, max(args.steps, 20))
+            res["rows"] = run_rows(torch, tb, inputs, dev, timer, l2, bufs, scales, geoms)
+        res["clocks_all"] = clk.summary()
+        res["clocks_timed"] = clk.summary(res["timed_window"])
     if world > 1:
-        tt = torch.tensor([ms_total], device=dev, dtype=torch.float64)
-        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
-        ms_total = float(tt.item())
-    per_launch = {key: statistics.median(e[0].elapsed_time(e[1]) for e in ev[key]) for key in ev}
-    spread = {}
-    for key in ev:
-        ts = sorted(e[0].elapsed_time(e[1]) for e in ev[key])
-        spread[key] = (ts[int(0.1 * (len(ts) - 1))], ts[int(0.9 * (len(ts) - 1))])
-    step_bytes = sum(packed_bytes(k) for k in KS for M in MS)
-    value = world * step_bytes * args.steps / (ms_total * 1e-3) / 1e9
+        tdist.barrier()
+        tdist.destroy_process_group()
+    return res
 
-    # ---- load-only floor: the same access pattern without decode (untimed for the metric) ----
-    floor = {}
-    fout = torch.empty(R, dtype=torch.int32, device=dev)
-    for k in KS:
-        for i in range(3):
-            tb.load_floor(bufs[k][i % len(bufs[k])], geoms[k], fout)
-        fa, fb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        n = max(20, len(bufs[k]) * 3)
-        fa.record(stream)
-        for i in range(n):
-            tb.load_floor(bufs[k][i % len(bufs[k])], geoms[k], fout)
-        fb.record(stream)
-        torch.cuda.synchronize(dev)
-        floor[k] = packed_bytes(k) / (fa.elapsed_time(fb) / n * 1e-3) / 1e9
 
-    # ---- end to end through the C ABI with host buffers (x in, out back) ----
-    # Every launch copies its x in from pinned host memory and its output back.  The copies run on
-    # their own streams so that they overlap the neighbouring launches: the x of each launch goes in
-    # ahead on the h2d stream, each output goes out on the d2h stream while the next launch runs.
-    # Each (k, M) slot has its own device buffers; events order the reuse of a slot across steps.
+def run_e2e(args, torch, tdist, tb, dev, stream, bufs, scales, geoms, xs, rot, world, sync_all):
+    """The headline through the C ABI with host buffers: every launch copies its x in from pinned host memory
+    and its output back.  The copies run on their own streams so that they overlap the neighbouring launches:
+    the x of each launch goes in ahead on the h2d stream, each output goes out on the d2h stream while the next
+    launch runs.  Each (k, M) slot has its own device buffers; events order the reuse of a slot across steps."""
     slots = [(k, M) for k in KS for M in MS]
     x_host = {M: xs[M].cpu().pin_memory() for M in MS}
     o_host = {s: torch.empty((s[1], R), dtype=torch.bfloat16).pin_memory() for s in slots}
@@ -280,117 +322,101 @@ def run_gpu(args):
         tt = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
         tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
         e2e_ms = float(tt.item())
-    h2d = sum(M * C * 2 for k in KS for M in MS)
-    d2h = sum(M * R * 2 for k in KS for M in MS)
-    e2e = {"value": world * step_bytes * args.steps / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
-
-    prefill = run_prefill(args, dev, stream, tb, inputs)
-    res = dict(value=value, ms_total=ms_total, per_launch=per_launch, spread=spread, load_floor=floor, e2e=e2e,
-               clocks=clk.summary(),
-               prefill=prefill, world=world, rank=rank, launches=len(KS) * len(MS) * args.steps)
-    if args.extra:
-        res["extra"] = run_extra(args, dev, stream, tb, inputs, l2)
-    if world > 1:
-        tdist.barrier()
-        tdist.destroy_process_group()
-    return res
+    step_bytes = sum(packed_bytes(k) for k in KS for M in MS)
+    return {"value": world * step_bytes * args.steps / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": sum(M * C * 2 for k in KS for M in MS),
+            "d2h_bytes_per_step": sum(M * R * 2 for k in KS for M in MS)}
 
 
-def run_prefill(args, dev, stream, tb, inputs):
-    """Prefill GEMM R=17408 C=5120 k=2 M=2048 (tcgen05) and the expand + cuBLAS comparator."""
-    import torch
-    k, M = 2, PREFILL_M
-    g = tb.Geometry(k, L, T, 1, R, C)
-    sets = [(_dev_words(inputs.random_words(inputs.SEED_CODES + 5000 + i, (R, C * k // 32)), dev),
-             _dev_bf16(inputs.normal_bf16(inputs.SEED_X + 5000 + i, (M, C)), dev)) for i in range(3)]
+def run_rows(torch, tb, inputs, dev, timer, l2, bufs, scales, geoms):
+    """Every other row of the hot path at its full size (see the module docstring).  Each entry: the row's
+    kind, k, M, mean and p10/p90 launch time, and its algorithmic bytes (matvecs, expand, floors) or FLOPs
+    (prefill); fractions are added by main() from the measured peaks."""
+    rows = []
+
+    def code_set(per_launch_bytes, k, seed, mult=1):
+        nrot = int(2 * l2 // per_launch_bytes) + 2
+        return [_dev_words(inputs.random_words(seed + 37 * i + k, (R, C * k // 32)), dev) for i in range(nrot * mult)]
+
     sc = _dev_f16(inputs.uniform_f16(inputs.SEED_SCALES, (R,)), dev)
-    out = torch.empty((M, R), dtype=torch.bfloat16, device=dev)
+
+    # ---- config 3: fused gate/up SwiGLU, two [17408, 5120] matrices ----
+    for k in (2, 3):
+        cs = code_set(2 * packed_bytes(k), k, 9000, 2)
+        g = tb.Geometry(k, L, T, 1, R, C)
+        for M in MS:
+            x = _dev_bf16(inputs.normal_bf16(inputs.SEED_X + M, (M, C)), dev)
+            o = torch.empty((M, R), dtype=torch.bfloat16, device=dev)
+            t = timer(lambda i: tb.gateup_swiglu(cs[2 * i], sc, cs[2 * i + 1], sc, x, g, o), len(cs) // 2)
+            rows.append({"kind": "gateup", "config": 3, "k": k, "M": M, **t,
+                         "bytes": 2 * packed_bytes(k) + 4 * R + 2 * M * C + 2 * M * R})
+        del cs
+    # ---- config 4: axis-0 down projection, stored W^T [17408 in, 5120 out] ----
+    for k in (2, 3):
+        cs = code_set(packed_bytes(k), k, 9500)
+        g = tb.Geometry(k, L, T, 0, R, C)
+        for M in MS:
+            x = _dev_bf16(inputs.normal_bf16(inputs.SEED_X + 10 + M, (M, R), 0.5), dev)
+            o = torch.empty((M, C), dtype=torch.bfloat16, device=dev)
+            ws = tb.new_workspace(M, g, dev)
+            t = timer(lambda i: tb.matvec_axis0(cs[i], sc, x, g, ws, o), len(cs))
+            rows.append({"kind": "axis0", "config": 4, "k": k, "M": M, **t,
+                         "bytes": packed_bytes(k) + 2 * R + 2 * M * R + 2 * M * C})
+        del cs
+    # ---- expand to bf16 (the transient of the comparator) ----
+    o = torch.empty((R, C), dtype=torch.bfloat16, device=dev)
+    for k in KS:
+        g = geoms[k]
+        t = timer(lambda i: tb.expand_bf16(bufs[k][i], scales[k], g, o), len(bufs[k]))
+        rows.append({"kind": "expand", "config": 2, "k": k, "M": 0, **t, "bytes": packed_bytes(k) + 2 * R + 2 * R * C})
+    del o
+    # ---- load-only floors of the packed stream (the M = 1 pattern, and fully coalesced) ----
+    fout = torch.empty(R, dtype=torch.int32, device=dev)
+    for k in KS:
+        for coal in (False, True):
+            t = timer(lambda i: tb.load_floor(bufs[k][i], geoms[k], fout, coalesced=coal), len(bufs[k]))
+            rows.append({"kind": "load_floor_coalesced" if coal else "load_floor", "config": 2, "k": k, "M": 0, **t,
+                         "bytes": packed_bytes(k) + 4 * R})
+    # ---- config 5: tensor-core prefill (axis 1, k = 2) and expand + cuBLAS ----
+    k = 2
+    g = tb.Geometry(k, L, T, 1, R, C)
     wtmp = torch.empty((R, C), dtype=torch.bfloat16, device=dev)
-    n = max(3, args.steps)
-
-    def timed(fn):
-        for i in range(3):
-            fn(i % 3)
-        torch.cuda.synchronize(dev)
-        es = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
-        for i in range(n):
-            es[i][0].record(stream)
-            fn(i % 3)
-            es[i][1].record(stream)
-        torch.cuda.synchronize(dev)
-        return statistics.median(a.elapsed_time(b) for a, b in es)
-
-    ms = timed(lambda i: tb.gemm_prefill(sets[i][0], sc, sets[i][1], g, out))
-    ms_cmp = timed(lambda i: torch.matmul(sets[i][1], tb.expand_bf16(sets[i][0], sc, g, wtmp).t()))
-    flops = 2.0 * M * R * C
-    return {"M": M, "k": k, "rows": R, "cols": C, "ms": ms, "tflops": flops / (ms * 1e-3) / 1e12,
-            "comparator": {"what": "trellis_expand_bf16 + torch.matmul (cuBLAS)", "ms": ms_cmp,
-                           "tflops": flops / (ms_cmp * 1e-3) / 1e12}}
-
-
-def run_extra(args, dev, stream, tb, inputs, l2):
-    """Other hot-path rows at their full sizes (informational; printed to stderr)."""
-    import torch
-    res = []
-    n = max(5, args.steps)
-
-    def timed(fn, nrot):
-        for i in range(3):
-            fn(i % nrot)
-        torch.cuda.synchronize(dev)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for i in range(n):
-            fn(i % nrot)
-        b.record(stream)
-        torch.cuda.synchronize(dev)
-        return a.elapsed_time(b) / n
-
-    # the decode MLP block (gate/up SwiGLU + down), replayed as CUDA graphs
+    cs = code_set(packed_bytes(k), k, 5000)
+    for M in PREFILL_M:
+        x = _dev_bf16(inputs.normal_bf16(inputs.SEED_X + 5000 + M, (M, C)), dev)
+        o = torch.empty((M, R), dtype=torch.bfloat16, device=dev)
+        t = timer(lambda i: tb.gemm_prefill(cs[i], sc, x, g, o), len(cs))
+        tc = timer(lambda i: torch.matmul(x, tb.expand_bf16(cs[i], sc, g, wtmp).t()), len(cs))
+        rows.append({"kind": "prefill", "config": 5, "k": k, "M": M, **t, "flops": 2.0 * M * R * C,
+                     "comparator": {"what": "trellis_expand_bf16 + torch.matmul (cuBLAS)", **tc}})
+    del cs
+    # ---- axis-0 prefill (the down projection for M > 4), k = 3, stored W^T [17408 in, 5120 out] ----
+    k = 3
+    g0 = tb.Geometry(k, L, T, 0, R, C)
+    cs = code_set(packed_bytes(k), k, 6000)
+    for M in PREFILL0_M:
+        x = _dev_bf16(inputs.normal_bf16(inputs.SEED_X + 6000 + M, (M, R), 0.5), dev)
+        o = torch.empty((M, C), dtype=torch.bfloat16, device=dev)
+        t = timer(lambda i: tb.gemm_prefill(cs[i], sc, x, g0, o), len(cs))
+        tc = timer(lambda i: torch.matmul(x, tb.expand_bf16(cs[i], sc, g0, wtmp)), len(cs))
+        rows.append({"kind": "prefill_axis0", "config": 5, "k": k, "M": M, **t, "flops": 2.0 * M * R * C,
+                     "comparator": {"what": "trellis_expand_bf16 + torch.matmul (cuBLAS)", **tc}})
+    del cs, wtmp
+    # ---- decode MLP block (gate/up SwiGLU + down) replayed as CUDA graphs ----
     for ku, kd in ((2, 2), (3, 3)):
         g_up, g_dn = tb.Geometry(ku, L, T, 1, R, C), tb.Geometry(kd, L, T, 0, R, C)
-        sc = _dev_f16(inputs.uniform_f16(inputs.SEED_SCALES, (R,)), dev)
         wsets = [[_dev_words(inputs.random_words(7000 + 10 * i + j, (R, C * (ku if j < 2 else kd) // 32)), dev)
                   for j in range(3)] for i in range(3)]
         for M in MS:
             graphs = [tb.MlpDecodeGraph(w[0], sc, w[1], sc, w[2], sc, g_up, g_dn, M) for w in wsets]
             for gr in graphs:
                 gr.x.copy_(_dev_bf16(inputs.normal_bf16(inputs.SEED_X, (M, C)), dev))
-            ms = timed(lambda i: graphs[i].replay(), len(graphs))
-            per = packed_bytes(ku) * 2 + packed_bytes(kd)
-            res.append({"kind": "mlp_graph", "k_up": ku, "k_down": kd, "M": M, "us": ms * 1e3,
-                        "packed_GBps": per / (ms * 1e-3) / 1e9})
+            t = timer(lambda i: graphs[i].replay(), len(graphs))
+            rows.append({"kind": "mlp_graph", "config": 3, "k": ku, "k_down": kd, "M": M, **t,
+                         "bytes": 2 * packed_bytes(ku) + packed_bytes(kd)})
             del graphs
         del wsets
-    for kind, ks in (("gateup", (2, 3)), ("axis0", (2, 3)), ("expand", (2, 3, 4))):
-        for k in ks:
-            per = packed_bytes(k) * (2 if kind == "gateup" else 1)
-            nrot = int(2 * l2 // per) + 2
-            cs = [_dev_words(inputs.random_words(9000 + 37 * i + k, (R, C * k // 32)), dev)
-                  for i in range(nrot * (2 if kind == "gateup" else 1))]
-            sc = _dev_f16(inputs.uniform_f16(inputs.SEED_SCALES, (R,)), dev)
-            g = tb.Geometry(k, L, T, 0 if kind == "axis0" else 1, R, C)
-            for M in ((1,) if kind == "expand" else MS):
-                if kind == "gateup":
-                    x = _dev_bf16(inputs.normal_bf16(inputs.SEED_X, (M, C)), dev)
-                    o = torch.empty((M, R), dtype=torch.bfloat16, device=dev)
-                    fn = lambda i: tb.gateup_swiglu(cs[2 * i], sc, cs[2 * i + 1], sc, x, g, o)
-                elif kind == "axis0":
-                    x = _dev_bf16(inputs.normal_bf16(inputs.SEED_X, (M, R), 0.5), dev)
-                    o = torch.empty((M, C), dtype=torch.bfloat16, device=dev)
-                    ws = tb.new_workspace(M, g, dev)
-                    fn = lambda i: tb.matvec_axis0(cs[i], sc, x, g, ws, o)
-                else:
-                    o = torch.empty((R, C), dtype=torch.bfloat16, device=dev)
-                    fn = lambda i: tb.expand_bf16(cs[i], sc, g, o)
-                ms = timed(fn, nrot)
-                row = {"kind": kind, "k": k, "M": M, "us": ms * 1e3, "packed_GBps": per / (ms * 1e-3) / 1e9}
-                if kind == "expand":
-                    row["bytes_GBps"] = (per + R * C * 2) / (ms * 1e-3) / 1e9
-                res.append(row)
-            del cs
-    return res
+    return rows
 
 
 def cpu_baseline(seconds: float = 12.0):
@@ -419,6 +445,27 @@ def cpu_baseline(seconds: float = 12.0):
     return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{n} random rows (of {R}) of each of the 12 (k, M) matvecs, {dt:.1f} s on one core",
             "per_row_s": dt / (n * len(KS) * len(MS))}
+
+
+def cpu_baseline_prefill(seconds: float = 10.0):
+    """The oracle's prefill (bf16 expand weights, double sums) on one host core for a bounded random sample of
+    output features of the M = 2048 prefill; TFLOP/s of the sampled outputs (2 * M * C per feature)."""
+    import oracle
+    from trellis_coded_weight_gb300 import inputs
+    oracle.build()
+    M = PREFILL_M[-1]
+    codes, scales, _ = inputs.make_linear(R, C, 2, 1, seed_codes=inputs.SEED_CODES + 5000)
+    x = inputs.normal_bf16(inputs.SEED_X + 5000 + M, (M, C))
+    t = time.perf_counter()
+    oracle.prefill(codes, scales, x, 2, L, T, rows=np.arange(2))
+    per = (time.perf_counter() - t) / 2
+    n = int(max(4, min(R, seconds / max(per, 1e-6))))
+    idx = np.sort(np.random.default_rng(2).choice(R, n, replace=False)).astype(np.int64)
+    t = time.perf_counter()
+    oracle.prefill(codes, scales, x, 2, L, T, rows=idx)
+    dt = time.perf_counter() - t
+    return {"value": 2.0 * M * C * n / dt / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} random output features (of {R}) x all {M} tokens of the k=2 prefill, {dt:.1f} s on one core"}
 
 
 _POOL_DATA = None
@@ -526,6 +573,8 @@ def run_single(kind: str, k: str, M: str):
     elif kind == "prefill0":  # axis-0 prefill: the stored W^T [R in][C out]
         x = _dev_bf16(inputs.normal_bf16(inputs.SEED_X, (M, R), 0.5), dev)
         fn = lambda: tb.gemm_prefill(codes, sc, x, g0)
+    elif kind in ("floor", "floor_rows"):
+        fn = lambda: tb.load_floor(codes, g1, coalesced=kind == "floor_rows")
     else:
         raise SystemExit(f"unknown kind {kind}")
     for _ in range(4):
@@ -534,22 +583,22 @@ def run_single(kind: str, k: str, M: str):
     print(json.dumps({"single": kind, "k": k, "M": M, "device_error": tb.device_error()}))
 
 
-def kernel_source_hash(name: str) -> str:
+def kernel_source_hash(*names: str) -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in (name, "common.cuh"):
+    for f in names + ("common.cuh",):
         with open(os.path.join(ROOT, "trellis_coded_weight_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def measured_traffic(kernel_file: str):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel's source changed since the capture."""
+def measured_profile(key: str):
+    """A committed ncu figure (DRAM bytes and instructions per launch) of a kernel, or None when the kernel's
+    source changed since the capture."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            d = json.load(f).get(kernel_file)
-        if d and d.get("source_hash") == kernel_source_hash(kernel_file):
+            d = json.load(f).get(key)
+        if d and d.get("source_hash") == kernel_source_hash(*d["sources"]):
             return d
     except Exception:
         pass
@@ -562,11 +611,11 @@ def main():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--extra", action="store_true", help="also time gate/up, axis-0 and expand (stderr)")
+    ap.add_argument("--all-rows", action="store_true", help="under torchrun, time the other rows on every rank")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--single", nargs=3, metavar=("KIND", "K", "M"),
                     help="profiling aid: run 4 launches of one kernel at full size and exit "
-                         "(KIND: axis1, gateup, axis0, expand, prefill, prefill0)")
+                         "(KIND: axis1, gateup, axis0, expand, prefill, prefill0, floor, floor_rows)")
     args = ap.parse_args()
     if args.single:
         run_single(*args.single)
@@ -585,46 +634,72 @@ def main():
         return
     peaks, peak_src = load_peaks()
     world = res["world"]
-    per = res["per_launch"]
-    # roofline of the dominant kernel (the axis-1 matvec; every timed launch is one).  The kernel is
-    # bound by the FMA-heavy pipe, not HBM: per weight the decode needs the 1MAD multiply and the
-    # byte sum (one lane-slot each) and the accumulation half a slot per input row (packed f32x2
-    # FMA); the pipe gives 16 lane-slots per clock per SM sub-partition.  The HBM view rides along.
-    import torch
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    sm_max_mhz = float(res["clocks"].get("sm_max_mhz") or 2070.0)
-    alg_ops = {(k, M): R * C * (2.0 + 0.5 * M) for k in KS for M in MS}
-    alg = {(k, M): packed_bytes(k) + 2 * R + 2 * M * C + 2 * M * R for k in KS for M in MS}
-    achieved_ops = sum(alg_ops.values()) / (sum(per.values()) * 1e-3) / 1e12
-    alu_peak = sms * 4 * 16 * sm_max_mhz * 1e6 / 1e12
-    achieved = sum(alg.values()) / (sum(per.values()) * 1e-3) / 1e9
     hbm = float(peaks["hbm_gbs"])
-    traffic = measured_traffic("matvec_axis1.cu")
-    roofline = {"kernel": "mv1_kernel (trellis_matvec_axis1)", "bound": "alu", "achieved": achieved_ops,
-                "peak": alu_peak, "unit": "T lane-slots/s (FMA-heavy pipe)", "frac": achieved_ops / alu_peak,
-                "peak_source": f"derived: {sms} SMs x 4 sub-partitions x 16 lanes x {sm_max_mhz:.0f} MHz",
-                "algorithmic_ops_per_launch": sum(alg_ops.values()) / len(alg_ops),
-                "traffic": (traffic["dram_bytes_per_launch"] if traffic else None),
-                "hbm": {"achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                        "peak_source": f"{peak_src} hbm_gbs",
-                        "algorithmic_bytes_per_launch": sum(alg.values()) / len(alg),
-                        "load_floor_GBps": {f"k{k}": res["load_floor"][k] for k in KS}}}
-    breakdown = [{"k": k, "M": M, "us": per[(k, M)] * 1e3,
+    bf16_peak = float(peaks["bf16_tflops"])
+    per = res["per_launch"]
+    alg = {(k, M): packed_bytes(k) + 2 * R + 2 * M * C + 2 * M * R for k in KS for M in MS}
+
+    # roofline of the dominant kernel: the axis-1 matvec (every timed launch is one).  Bound by HBM in the
+    # metric's terms: algorithmic bytes per launch over the mean launch time against the measured copy rate.
+    achieved = sum(alg.values()) / (sum(per.values()) * 1e-3) / 1e9
+    prof = [measured_profile(f"axis1_k{k}_M{M}") for k in KS for M in MS]
+    traffic = (sum(p["dram_bytes_per_launch"] for p in prof) / len(prof)) if all(prof) else None
+    floors = {r["kind"] + f"_k{r['k']}": packed_bytes(r["k"]) / (r["us"] * 1e-6) / 1e9
+              for r in res.get("rows", []) if r["kind"].startswith("load_floor")}
+    roofline = {"kernel": "trellis_matvec_axis1 (mv1_kernel at M = 1, mvtc_kernel at M >= 2)", "bound": "hbm",
+                "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "peak_source": f"{peak_src} hbm_gbs (copy)",
+                "algorithmic_bytes_per_launch": sum(alg.values()) / len(alg),
+                "traffic": traffic, "load_floor_GBps": floors}
+    if all(prof):
+        # issue view: the warp-instructions ncu counted per launch, over the mean launch time, against one
+        # instruction per cycle per SM sub-partition at the maximum SM clock
+        import torch
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        mhz = float(res["clocks_all"].get("sm_max_mhz") or 2070.0)
+        inst = sum(p["warp_instructions_per_launch"] for p in prof)
+        ach = inst / (sum(per.values()) * 1e-3) / 1e12
+        peak_i = sms * 4 * mhz * 1e6 / 1e12
+        roofline["issue"] = {"achieved": ach, "peak": peak_i, "unit": "T warp-instructions/s", "frac": ach / peak_i,
+                             "peak_source": f"derived: {sms} SMs x 4 schedulers x 1 instruction/clock x {mhz:.0f} MHz",
+                             "instructions_per_weight": inst * 32 / (R * C * len(alg)),
+                             "source": "ncu smsp__inst_executed.sum, profiles/traffic.json"}
+    breakdown = [{"kind": "axis1", "config": 2, "k": k, "M": M, "us": per[(k, M)] * 1e3,
                   "us_p10_p90": [res["spread"][(k, M)][0] * 1e3, res["spread"][(k, M)][1] * 1e3],
+                  "bytes": alg[(k, M)], "GBps": alg[(k, M)] / (per[(k, M)] * 1e-3) / 1e9,
                   "packed_GBps": packed_bytes(k) / (per[(k, M)] * 1e-3) / 1e9,
-                  "frac_hbm": packed_bytes(k) / (per[(k, M)] * 1e-3) / 1e9 / hbm} for k in KS for M in MS]
-    pf = res["prefill"]
-    pf["frac"] = pf["tflops"] / float(peaks["bf16_tflops"])
-    pf["peak"] = float(peaks["bf16_tflops"])
-    pf["peak_source"] = f"{peak_src} bf16_tflops (burst)"
+                  "frac_hbm": alg[(k, M)] / (per[(k, M)] * 1e-3) / 1e9 / hbm} for k in KS for M in MS]
+    prefill = None
+    for r in res.get("rows", []):
+        if "bytes" in r:
+            r["GBps"] = r["bytes"] / (r["us"] * 1e-6) / 1e9
+            r["frac_hbm"] = r["GBps"] / hbm
+            if r["kind"] in ("gateup", "axis0", "mlp_graph"):
+                packed = (2 * packed_bytes(r["k"]) if r["kind"] == "gateup" else packed_bytes(r["k"]))
+                if r["kind"] == "mlp_graph":
+                    packed = 2 * packed_bytes(r["k"]) + packed_bytes(r["k_down"])
+                r["packed_GBps"] = packed / (r["us"] * 1e-6) / 1e9
+        else:
+            r["TFLOPs"] = r["flops"] / (r["us"] * 1e-6) / 1e12
+            r["frac_bf16"] = r["TFLOPs"] / bf16_peak
+            r["comparator"]["TFLOPs"] = r["flops"] / (r["comparator"]["us"] * 1e-6) / 1e12
+            if r["kind"] == "prefill" and r["M"] == PREFILL_M[-1]:
+                prefill = {"M": r["M"], "k": r["k"], "rows": R, "cols": C, "ms": r["us"] * 1e-3, "tflops": r["TFLOPs"],
+                           "frac": r["frac_bf16"], "peak": bf16_peak, "peak_source": f"{peak_src} bf16_tflops (burst)",
+                           "comparator": {"what": r["comparator"]["what"], "ms": r["comparator"]["us"] * 1e-3,
+                                          "tflops": r["comparator"]["TFLOPs"]}}
+        breakdown.append(r)
+    clocks = dict(res["clocks_all"])
+    clocks["window"] = "from the first warm-up step to the last timed row"
+    clocks["timed_region"] = res["clocks_timed"]
     line = {
         "metric": METRIC, "value": res["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": res["ms_total"] / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic: seeded SplitMix64 code words, fp16 scales U[0.005,0.02], bf16 x ~ N(0,1)",
         "config": workload_desc(), "frac_hbm": res["value"] / world / hbm,
-        "roofline": roofline, "e2e": res["e2e"], "gpu_launches": res["launches"], "clocks": res["clocks"],
-        "prefill": pf, "breakdown": breakdown,
+        "roofline": roofline, "e2e": res["e2e"], "gpu_launches": res["launches"], "clocks": clocks,
+        "prefill": prefill, "breakdown": breakdown,
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
@@ -632,8 +707,10 @@ def main():
             line["cpu_baseline"]["all_cores"] = cpu_baseline_all_cores(line["cpu_baseline"].pop("per_row_s"))
         except Exception as e:  # the single-core figure stands on its own
             line["cpu_baseline"]["all_cores"] = {"unavailable": str(e)[:200]}
-    if "extra" in res:
-        print(json.dumps({"extra": res["extra"]}), file=sys.stderr, flush=True)
+        try:
+            line["cpu_baseline"]["prefill"] = cpu_baseline_prefill()
+        except Exception as e:
+            line["cpu_baseline"]["prefill"] = {"unavailable": str(e)[:200]}
     print(json.dumps(line), flush=True)
 
 

@@ -245,8 +245,8 @@ int trellis_gemm_prefill(const uint32_t *codes, const uint16_t *scales, const ui
 /*
  * trellis_load_floor -- measurement aid with no counterpart in the pages'
  * operations: reads an axis-1 bitstream with exactly the access pattern of
- * trellis_matvec_axis1 (one lane per stored row, 16-byte loads of half
- * blocks) and decodes nothing; out[r] = XOR of every word it loads for
+ * trellis_matvec_axis1 at M = 1 (one lane per stored row, 16-byte loads of
+ * half blocks) and decodes nothing; out[r] = XOR of every word it loads for
  * stored row r: each block's words plus the spill reads of its words 4k and
  * 0, i.e. the XOR of the row's words other than words 0 and 4k of each block.
  * Its bandwidth is the HBM rate that access pattern can reach, the floor
@@ -256,6 +256,19 @@ int trellis_gemm_prefill(const uint32_t *codes, const uint16_t *scales, const ui
  * EGEOM, EAXIS, ENULL, EALIGN, EDEVICE, ECUDA (launch).
  */
 int trellis_load_floor(const uint32_t *codes, uint32_t *out, const trellis_geom_t *g, trellis_stream_t stream);
+
+/*
+ * trellis_load_floor_rows -- measurement aid with no counterpart in the
+ * pages' operations: reads the same axis-1 bitstream fully coalesced (one
+ * warp per stored row, its lanes on consecutive 16-byte chunks of the row,
+ * warps striding over the rows in one wave) and decodes nothing;
+ * out[r] = XOR of all words of stored row r.  Its bandwidth is what the best
+ * access pattern reaches on HBM for a stream of this size.
+ *   codes [rows][cols*k/32] (device, 16-byte aligned)   out [rows] uint32 (device)
+ * Requires a valid axis-1 geometry without the interleaved layout.  Errors:
+ * EGEOM, EAXIS, ENULL, EALIGN, EDEVICE, ECUDA (launch).
+ */
+int trellis_load_floor_rows(const uint32_t *codes, uint32_t *out, const trellis_geom_t *g, trellis_stream_t stream);
 
 /*
  * trellis_prefill_plan -- the tile plan trellis_gemm_prefill follows for

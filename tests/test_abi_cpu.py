@@ -123,9 +123,11 @@ def test_interleaved_geometry_rules(lib, kw, ok):
     assert (lib.trellis_check_geom(ctypes.byref(G(**kw))) == 0) == ok
 
 
-def test_load_floor_errors_before_launch(lib):
+@pytest.mark.parametrize("fn", ["trellis_load_floor", "trellis_load_floor_rows"])
+def test_load_floor_errors_before_launch(lib, fn):
     gu = G(axis=1)
-    assert lib.trellis_load_floor(A, A, ctypes.byref(G(axis=0)), None) == -4  # EAXIS
-    assert lib.trellis_load_floor(None, A, ctypes.byref(gu), None) == -7      # ENULL
-    assert lib.trellis_load_floor(A + 4, A, ctypes.byref(gu), None) == -3     # EALIGN
-    assert lib.trellis_load_floor(A, A, ctypes.byref(G(axis=1, cols=100)), None) == -1  # EGEOM
+    f = getattr(lib, fn)
+    assert f(A, A, ctypes.byref(G(axis=0)), None) == -4  # EAXIS
+    assert f(None, A, ctypes.byref(gu), None) == -7      # ENULL
+    assert f(A + 4, A, ctypes.byref(gu), None) == -3     # EALIGN
+    assert f(A, A, ctypes.byref(G(axis=1, cols=100)), None) == -1  # EGEOM

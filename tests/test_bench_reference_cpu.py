@@ -40,15 +40,16 @@ def test_reference_arm_other_ranks_print_nothing():
     assert _run({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}) == []
 
 
-def test_traffic_counters_only_for_the_source_they_were_taken_on(monkeypatch):
-    # roofline.traffic comes from the committed ncu summary only while the kernel source hash matches it
+def test_profile_counters_only_for_the_source_they_were_taken_on(monkeypatch):
+    # roofline.traffic and the issue view come from the committed ncu figures only while the kernel source
+    # hash matches the one they were taken on
     import bench
-    d = bench.measured_traffic("matvec_axis1.cu")
-    if d is None:  # the source changed since the capture: the bench reports traffic null, as it should
-        pytest.skip("profiles/traffic.json was taken on another matvec_axis1.cu / common.cuh")
-    algorithmic = [bench.R * bench.C * k / 8 + 2 * bench.R + 2 * M * bench.C + 2 * M * bench.R
-                   for k in bench.KS for M in bench.MS]
-    per = [d["per_launch"][f"k{k}_M{M}"] for k in bench.KS for M in bench.MS]
-    assert all(0.99 <= p / a <= 1.01 for p, a in zip(per, algorithmic)), "DRAM traffic equals algorithmic bytes"
-    monkeypatch.setattr(bench, "kernel_source_hash", lambda name: "0" * 16)
-    assert bench.measured_traffic("matvec_axis1.cu") is None
+    prof = {(k, M): bench.measured_profile(f"axis1_k{k}_M{M}") for k in bench.KS for M in bench.MS}
+    if not all(prof.values()):  # the source changed since the capture: the bench reports traffic null
+        pytest.skip("profiles/traffic.json was taken on other axis-1 kernel sources")
+    for (k, M), d in prof.items():
+        algorithmic = bench.R * bench.C * k / 8 + 2 * bench.R + 2 * M * bench.C + 2 * M * bench.R
+        assert 0.99 <= d["dram_bytes_per_launch"] / algorithmic <= 1.01, "DRAM traffic equals algorithmic bytes"
+        assert d["warp_instructions_per_launch"] > 0
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda *names: "0" * 16)
+    assert bench.measured_profile("axis1_k2_M1") is None

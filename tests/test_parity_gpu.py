@@ -233,3 +233,22 @@ def test_matvec_axis0_is_deterministic():
     a = tb.matvec_axis0(*args).clone()
     b = tb.matvec_axis0(*args)
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+# ------------------------------------------------------------------ load-only floors (measurement aids)
+
+@pytest.mark.parametrize("k", [2, 3, 4])
+def test_load_floors_fold_the_words_they_read(k):
+    """Both floors read the stream and fold every loaded word by XOR: the coalesced floor all words of the
+    row; the M = 1 pattern each block's words plus the spill reads of words 4k and 0, which cancel those two."""
+    rows, cols = 300, 1280
+    codes, _, _ = inputs.make_linear(rows, cols, k, 1, seed_codes=600 + k)
+    g = tb.Geometry(k, L, T, 1, rows, cols)
+    dc = to_dev_u32(codes)
+    got = tb.load_floor(dc, g, coalesced=True).cpu().numpy().view(np.uint32)
+    assert np.array_equal(got, np.bitwise_xor.reduce(codes, axis=1))
+    wpb = 8 * k
+    keep = np.ones(wpb, dtype=bool)
+    keep[0] = keep[4 * k] = False
+    want = np.bitwise_xor.reduce(codes.reshape(rows, -1, wpb)[:, :, keep].reshape(rows, -1), axis=1)
+    assert np.array_equal(tb.load_floor(dc, g).cpu().numpy().view(np.uint32), want)

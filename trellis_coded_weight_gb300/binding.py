@@ -28,7 +28,7 @@ STATUS_NAMES = {0: "TRELLIS_OK", -1: "TRELLIS_EGEOM", -2: "TRELLIS_EM", -3: "TRE
 EXPORTS = ("trellis_abi_version", "trellis_status_string", "trellis_check_geom", "trellis_expand_bf16",
            "trellis_matvec_axis1", "trellis_matvec_axis0", "trellis_workspace_bytes", "trellis_gateup_swiglu",
            "trellis_gemm_prefill", "trellis_device_error", "trellis_mlp_decode", "trellis_matvec_axis1_bf16w",
-           "trellis_matvec_axis0_bf16w", "trellis_load_floor", "trellis_prefill_plan")
+           "trellis_matvec_axis0_bf16w", "trellis_load_floor", "trellis_load_floor_rows", "trellis_prefill_plan")
 
 
 class TrellisGeom(ctypes.Structure):
@@ -111,6 +111,8 @@ def load(path: str = LIB_PATH):
             lib.trellis_device_error.argtypes = [i32]
             lib.trellis_load_floor.restype = i32
             lib.trellis_load_floor.argtypes = [vp, vp, g, vp]
+            lib.trellis_load_floor_rows.restype = i32
+            lib.trellis_load_floor_rows.argtypes = [vp, vp, g, vp]
             lib.trellis_prefill_plan.restype = i32
             lib.trellis_prefill_plan.argtypes = [i32, g, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
             _lib = lib
@@ -238,14 +240,16 @@ def gemm_prefill(codes, scales, x, g: Geometry, out=None):
     return out
 
 
-def load_floor(codes: torch.Tensor, g: Geometry, out: torch.Tensor = None) -> torch.Tensor:
-    """Measurement aid: read the axis-1 stream with the matvec's access pattern, decode nothing;
-    out[r] = XOR of every word loaded for row r (int32 view of uint32)."""
+def load_floor(codes: torch.Tensor, g: Geometry, out: torch.Tensor = None, coalesced: bool = False) -> torch.Tensor:
+    """Measurement aid: read the axis-1 stream and decode nothing; out[r] = XOR of the words loaded for row r
+    (int32 view of uint32).  Default: the M = 1 matvec's access pattern (lane per row); coalesced: a warp per
+    row with its lanes on consecutive 16-byte chunks."""
     if out is None:
         out = torch.empty(g.rows, dtype=torch.int32, device=codes.device)
     args = (_req(codes, "codes", _CODES, g.codes_shape), _req(out, "out", (torch.int32,), (g.rows,)))
+    fn = "trellis_load_floor_rows" if coalesced else "trellis_load_floor"
     with _on(codes):
-        _check("trellis_load_floor", load().trellis_load_floor(*args, ctypes.byref(g.c()), _stream(codes)))
+        _check(fn, getattr(load(), fn)(*args, ctypes.byref(g.c()), _stream(codes)))
     return out
 
 

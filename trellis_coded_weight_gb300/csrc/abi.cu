@@ -251,6 +251,18 @@ int trellis_load_floor(const uint32_t* codes, uint32_t* out, const trellis_geom_
       trellis::launch_load_floor(codes, out, g->k, g->rows, g->cols, static_cast<cudaStream_t>(stream)));
 }
 
+int trellis_load_floor_rows(const uint32_t* codes, uint32_t* out, const trellis_geom_t* g, trellis_stream_t stream) {
+  int st = trellis_check_geom(g);
+  if (st) return st;
+  if (g->axis != 1) return TRELLIS_EAXIS;
+  if (g->interleave) return TRELLIS_EGEOM;
+  if (!codes || !out) return TRELLIS_ENULL;
+  if (!aligned16(codes) || !aligned16(out)) return TRELLIS_EALIGN;
+  if ((st = device_ok())) return st;
+  return cuda_status(
+      trellis::launch_load_floor_rows(codes, out, g->k, g->rows, g->cols, static_cast<cudaStream_t>(stream)));
+}
+
 int trellis_device_error(int reset) {
   int st = device_ok();
   if (st) return st;

@@ -14,9 +14,26 @@ constexpr int kT_host = 256;  // positions per block, the only T the kernels sup
 cudaError_t launch_expand_bf16(const uint32_t* codes, const uint16_t* scales, uint16_t* out, int k, int L,
                                int64_t rows, int64_t cols, int interleave, cudaStream_t st);
 
+// Axis-1 matvec and fused gate/up (matvec_axis1_tc.cu): M = 1 on the CUDA cores, M >= 2 with y*x accumulated
+// on the tensor cores.  The _tc and _fma forms take one path for every M.
 cudaError_t launch_matvec_axis1(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
                                 uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols,
                                 cudaStream_t st);
+cudaError_t launch_matvec_axis1_tc(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
+                                   uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols,
+                                   cudaStream_t st);
+cudaError_t launch_gateup_swiglu_tc(const uint32_t* gcodes, const uint16_t* gscales, const uint32_t* ucodes,
+                                    const uint16_t* uscales, const uint16_t* x, uint16_t* out, int M, int k,
+                                    int L, int64_t rows, int64_t cols, cudaStream_t st);
+// The same two layers with the accumulation on the CUDA cores (packed fp32 FMA, matvec_axis1.cu).
+cudaError_t launch_matvec_axis1_fma(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
+                                    uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols,
+                                    cudaStream_t st);
+cudaError_t launch_gateup_swiglu_fma(const uint32_t* gcodes, const uint16_t* gscales, const uint32_t* ucodes,
+                                     const uint16_t* uscales, const uint16_t* x, uint16_t* out, int M, int k,
+                                     int L, int64_t rows, int64_t cols, cudaStream_t st);
+// Warps per CTA of the CUDA-core axis-1 kernel for a row of nb blocks at the given register count.
+int mv1_splits(int nb, int regs);
 
 // The same matvecs with bf16-rounded weights (bf16(value * scale) before the FMA).
 cudaError_t launch_matvec_axis1_bf16w(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
@@ -55,6 +72,9 @@ int device_sm_count();
 // Load-only floor of the axis-1 access pattern (no decode): out[r] = XOR of row r's words.
 cudaError_t launch_load_floor(const uint32_t* codes, uint32_t* out, int k, int64_t rows, int64_t cols,
                               cudaStream_t st);
+// Coalesced load floor: a warp per stored row, lanes on consecutive 16-byte chunks.
+cudaError_t launch_load_floor_rows(const uint32_t* codes, uint32_t* out, int k, int64_t rows, int64_t cols,
+                                   cudaStream_t st);
 
 // Device error word of the tensor-core kernels (bounded waits that gave up).
 int read_device_error(int reset);

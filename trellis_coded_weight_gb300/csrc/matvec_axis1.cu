@@ -185,12 +185,19 @@ __global__ void __launch_bounds__(512) mv1_kernel(const Mv1Params p) {
 // Warps per CTA (the row's half blocks are split S ways): as many as keep
 // four CTAs resident per SM with this instantiation's register count, so the
 // R/32 CTAs of a large matrix run in a single wave; never more than the row
-// has half blocks, and at most 16.
-static int mv1_splits(int nb, int regs) {
-  int s = 65536 / (4 * 32 * (regs > 0 ? regs : 64));
+// has half blocks, and at most 16.  Registers are allocated per thread in
+// units of 8, so the count is rounded up first.  Among the counts within a
+// quarter of that bound, one that divides the half blocks evenly is taken, so
+// that no warp of the CTA has a half block more than the others.
+int mv1_splits(int nb, int regs) {
+  const int r8 = ((regs > 0 ? regs : 64) + 7) & ~7;
+  int s = 65536 / (4 * 32 * r8);
   if (s > 2 * nb) s = 2 * nb;
   if (s > 16) s = 16;
-  return s < 1 ? 1 : s;
+  if (s < 1) s = 1;
+  for (int c = s; c * 4 >= s * 3; --c)
+    if ((2 * nb) % c == 0) return c;
+  return s;
 }
 
 template <int K, int L, int M, bool GU, bool BW>
@@ -278,9 +285,51 @@ cudaError_t launch_load_floor(const uint32_t* codes, uint32_t* out, int k, int64
   return cudaGetLastError();
 }
 
-cudaError_t launch_matvec_axis1(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
-                                uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols,
-                                cudaStream_t st) {
+// Coalesced load floor: a warp reads whole stored rows, its lanes on consecutive 16-byte chunks of the row
+// (a row of 1280-2560 bytes in 3-5 requests), warps striding over the rows in a single wave; every word is
+// folded by XOR so the loads stay live.  Its bandwidth is what a fully coalesced read of the same stream
+// reaches at this size.
+__global__ void __launch_bounds__(256) load_floor_rows_kernel(const uint4* codes, uint32_t* out, int64_t R,
+                                                               int chunks) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < R; r += nwarps) {
+    const uint4* row = codes + r * chunks;
+    uint32_t acc = 0;
+    for (int c = lane; c < chunks; c += 32) {
+      const uint4 v = __ldg(row + c);
+      acc ^= v.x ^ v.y ^ v.z ^ v.w;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc ^= __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+    if (lane == 0) out[r] = acc;
+  }
+}
+
+cudaError_t launch_load_floor_rows(const uint32_t* codes, uint32_t* out, int k, int64_t rows, int64_t cols,
+                                   cudaStream_t st) {
+  static PerDevice<int> per_sm_of;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
+  const int per_sm = per_sm_of.get(dev, [] {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, load_floor_rows_kernel, 256, 0) != cudaSuccess) {
+      cudaGetLastError();
+      n = 1;
+    }
+    return n < 1 ? 1 : n;
+  }, 1);
+  const int chunks = (int)(cols * k / 128);  // 16-byte chunks per row (cols is a multiple of 256)
+  int64_t grid = (int64_t)device_sm_count() * per_sm;
+  const int64_t need = (rows + 7) / 8;
+  if (grid > need) grid = need;
+  load_floor_rows_kernel<<<(unsigned)grid, 256, 0, st>>>(reinterpret_cast<const uint4*>(codes), out, rows, chunks);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_matvec_axis1_fma(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
+                                    uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols,
+                                    cudaStream_t st) {
   Mv1Params p{};
   p.codes[0] = p.codes[1] = codes;
   p.scales[0] = p.scales[1] = scales;
@@ -298,9 +347,9 @@ cudaError_t launch_matvec_axis1_bf16w(const uint32_t* codes, const uint16_t* sca
   return mv1_dispatch<false, true>(p, k, L, M, st);
 }
 
-cudaError_t launch_gateup_swiglu(const uint32_t* gcodes, const uint16_t* gscales, const uint32_t* ucodes,
-                                 const uint16_t* uscales, const uint16_t* x, uint16_t* out, int M, int k,
-                                 int L, int64_t rows, int64_t cols, cudaStream_t st) {
+cudaError_t launch_gateup_swiglu_fma(const uint32_t* gcodes, const uint16_t* gscales, const uint32_t* ucodes,
+                                     const uint16_t* uscales, const uint16_t* x, uint16_t* out, int M, int k,
+                                     int L, int64_t rows, int64_t cols, cudaStream_t st) {
   Mv1Params p{};
   p.codes[0] = gcodes; p.codes[1] = ucodes;
   p.scales[0] = gscales; p.scales[1] = uscales;
