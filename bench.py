@@ -31,6 +31,7 @@ sample of rows of the same workload.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import os
 import statistics
@@ -210,11 +211,26 @@ def run_gpu(args):
     xs = {M: _dev_bf16(inputs.normal_bf16(inputs.SEED_X + M, (M, C)), dev) for M in MS}
     outs = {M: torch.empty((M, R), dtype=torch.bfloat16, device=dev) for M in MS}
     rot = {k: 0 for k in KS}
+    # The headline calls the C entry point directly with its arguments prepared once (pointers, geometry,
+    # stream), so that the host issues launches faster than the GPU runs them; the e2e leg below goes through
+    # the Python binding.  The binding's own checks ran on these tensors during set-up.
+    lib = tb.load()
+    sptr = stream.cuda_stream
+    cargs = {}
+    for k in KS:
+        for M in MS:
+            tb.matvec_axis1(bufs[k][0], scales[k], xs[M], geoms[k], outs[M])
+            for i, b in enumerate(bufs[k]):
+                cargs[(k, M, i)] = (b.data_ptr(), scales[k].data_ptr(), xs[M].data_ptr(), outs[M].data_ptr(), M,
+                                    ctypes.byref(geoms[k].c()), sptr)
+    fn_mv = lib.trellis_matvec_axis1
 
     def launch(k, M):
         i = rot[k]
         rot[k] = (i + 1) % len(bufs[k])
-        tb.matvec_axis1(bufs[k][i], scales[k], xs[M], geoms[k], outs[M])
+        st = fn_mv(*cargs[(k, M, i)])
+        if st:
+            raise RuntimeError(f"trellis_matvec_axis1 returned {st}")
 
     def step(events=None):
         for k in KS:
@@ -234,15 +250,13 @@ def run_gpu(args):
     with ClockSampler(local) as clk:
         for _ in range(args.warmup):
             step()
-        # ---- timed region: exactly K steps, per-launch events on the launch stream ----
-        ev = {(k, M): [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-              for k in KS for M in MS}
+        # ---- timed region: exactly K steps, one event pair around them ----
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         sync_all()
         h0 = time.time()
         t0.record(stream)
-        for s in range(args.steps):
-            step({key: ev[key][s] for key in ev})
+        for _ in range(args.steps):
+            step()
         t1.record(stream)
         sync_all()
         h1 = time.time()
@@ -251,6 +265,13 @@ def run_gpu(args):
             tt = torch.tensor([ms_total], device=dev, dtype=torch.float64)
             tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
             ms_total = float(tt.item())
+        # ---- the same K steps again with an event pair around every launch: each kernel's mean duration ----
+        ev = {(k, M): [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+              for k in KS for M in MS}
+        sync_all()
+        for s in range(args.steps):
+            step({key: ev[key][s] for key in ev})
+        sync_all()
         per_launch, spread = {}, {}
         for key in ev:
             ts = sorted(e[0].elapsed_time(e[1]) for e in ev[key])

@@ -11,6 +11,7 @@ torch.int32 or torch.uint32 tensors holding the packed words.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -50,7 +51,12 @@ class Geometry:
     interleave: int = 0  # 2: the k=3 axis-0 layout [cols/512][rows][48]
 
     def c(self) -> TrellisGeom:
-        return TrellisGeom(self.k, self.L, self.T, self.axis, self.rows, self.cols, self.interleave, 0)
+        """The C struct of this geometry (built once per geometry and kept)."""
+        g = _GEOM_STRUCTS.get(self)
+        if g is None:
+            g = _GEOM_STRUCTS.setdefault(self, TrellisGeom(self.k, self.L, self.T, self.axis, self.rows, self.cols,
+                                                           self.interleave, 0))
+        return g
 
     @property
     def words_per_row(self) -> int:
@@ -61,6 +67,9 @@ class Geometry:
         if self.interleave:
             return (self.cols // (2 * self.T), self.rows, 2 * self.T * self.k // 32)
         return (self.rows, self.words_per_row)
+
+
+_GEOM_STRUCTS: dict = {}
 
 
 class TrellisError(RuntimeError):
@@ -131,6 +140,8 @@ def _stream(t: torch.Tensor) -> int:
 def _on(t: torch.Tensor):
     """Make the tensor's device current for the C call: the library reads the
     current device (its SM count, kernel attributes) and launches on it."""
+    if t.device.index == torch.cuda.current_device():
+        return contextlib.nullcontext()
     return torch.cuda.device(t.device)
 
 
