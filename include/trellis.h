@@ -295,6 +295,20 @@ int trellis_prefill_plan(int M, const trellis_geom_t *g, int sms, int *tokens_pe
  */
 int trellis_device_error(int reset);
 
+/*
+ * trellis_set_wait_limit -- diagnostic with no counterpart in the pages:
+ * sets the limit of each bounded wait in the tensor-core kernel
+ * (trellis_gemm_prefill) for launches issued after the call, in
+ * nanoseconds of the GPU's global timer; 0 restores the default (2 s).
+ * It exists so that tests can make the waits run out on an ordinary
+ * problem and check the error path: the kernel then records a non-zero
+ * code (trellis_device_error), lets its copies and MMAs already issued
+ * finish, and returns with the context intact; its output is undefined.
+ * The setting is process-wide and applies to every device.  Returns
+ * TRELLIS_OK.
+ */
+int trellis_set_wait_limit(uint64_t nanoseconds);
+
 #ifdef __cplusplus
 }
 #endif

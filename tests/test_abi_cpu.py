@@ -131,3 +131,10 @@ def test_load_floor_errors_before_launch(lib, fn):
     assert f(None, A, ctypes.byref(gu), None) == -7      # ENULL
     assert f(A + 4, A, ctypes.byref(gu), None) == -3     # EALIGN
     assert f(A, A, ctypes.byref(G(axis=1, cols=100)), None) == -1  # EGEOM
+
+
+def test_wait_limit_setter_needs_no_device(lib):
+    # a host-side setting read by later prefill launches; 0 restores the default
+    lib.trellis_set_wait_limit.argtypes = [ctypes.c_uint64]
+    assert lib.trellis_set_wait_limit(1000) == 0
+    assert lib.trellis_set_wait_limit(0) == 0

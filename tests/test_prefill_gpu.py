@@ -137,3 +137,38 @@ def test_prefill_axis0_leftover_tiles_one_stage(oracle_mod):
     idx = np.unique(np.r_[np.arange(0, cols, 89), 127, 128, 5247, 5248, cols - 1]).astype(np.int64)
     ref, ab = oracle_mod.matvec_axis0_bf16w(codes, scales, x, k, L, T, cols=idx)
     check_band(oracle_mod, bf16_bits(out)[:, idx], ref, ab, f"prefill axis0 one-stage leftover M={M}")
+
+
+# ------------------------------------------------------------------ bounded waits (failure detection)
+
+@pytest.mark.parametrize("axis,M", [(1, 40), (0, 24)])
+def test_bounded_waits_run_out_and_the_next_call_is_correct(oracle_mod, axis, M):
+    """Failure detection without a GPU fault: with every pipeline wait limited to 200 ns the waits of an
+    ordinary problem run out; the kernel records a non-zero error word, lets its copies and MMAs finish and
+    returns with the context intact.  The next call, at the default limit, is correct and clean.  Axis 0 at
+    M = 24 runs the cluster-split reduction (8-CTA clusters), whose waits run out too."""
+    rows, cols, k = 512, 2048, 2
+    codes, scales, _ = inputs.make_linear(rows, cols, k, 1, seed_codes=880 + axis, seed_scales=881)
+    n_in = cols if axis == 1 else rows
+    x = inputs.normal_bf16(882 + axis, (M, n_in), 1.0 if axis == 1 else 0.5)
+    g = tb.Geometry(k, L, T, axis, rows, cols)
+    dc, ds, dx = to_dev_u32(codes), to_dev_f16(scales), to_dev_bf16(x)
+    tb.device_error(reset=True)
+    try:
+        tb.set_wait_limit(200)
+        tb.gemm_prefill(dc, ds, dx, g)
+        torch.cuda.synchronize()  # a clean return: no CUDA error
+    finally:
+        tb.set_wait_limit(0)
+    assert tb.device_error(reset=True) != 0, "no bounded wait ran out at a 200 ns limit"
+    out = tb.gemm_prefill(dc, ds, dx, g)
+    torch.cuda.synchronize()
+    assert tb.device_error() == 0
+    if axis == 1:
+        ref, ab = oracle_mod.prefill(codes, scales, x, k, L, T)
+    else:
+        ref, ab = oracle_mod.matvec_axis0_bf16w(codes, scales, x, k, L, T)
+    check_band(oracle_mod, bf16_bits(out), ref, ab, f"prefill axis{axis} after a run-out")
+    bn, plan = tb.prefill_plan(M, g)
+    if axis == 0:
+        assert plan[0][2] > 1, "the axis-0 case is meant to run the cluster split"

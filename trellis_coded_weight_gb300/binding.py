@@ -29,7 +29,8 @@ STATUS_NAMES = {0: "TRELLIS_OK", -1: "TRELLIS_EGEOM", -2: "TRELLIS_EM", -3: "TRE
 EXPORTS = ("trellis_abi_version", "trellis_status_string", "trellis_check_geom", "trellis_expand_bf16",
            "trellis_matvec_axis1", "trellis_matvec_axis0", "trellis_workspace_bytes", "trellis_gateup_swiglu",
            "trellis_gemm_prefill", "trellis_device_error", "trellis_mlp_decode", "trellis_matvec_axis1_bf16w",
-           "trellis_matvec_axis0_bf16w", "trellis_load_floor", "trellis_load_floor_rows", "trellis_prefill_plan")
+           "trellis_matvec_axis0_bf16w", "trellis_load_floor", "trellis_load_floor_rows", "trellis_prefill_plan",
+           "trellis_set_wait_limit")
 
 
 class TrellisGeom(ctypes.Structure):
@@ -118,6 +119,8 @@ def load(path: str = LIB_PATH):
             lib.trellis_mlp_decode.argtypes = [vp] * 9 + [i32, g, g, vp, sz, vp]
             lib.trellis_device_error.restype = i32
             lib.trellis_device_error.argtypes = [i32]
+            lib.trellis_set_wait_limit.restype = i32
+            lib.trellis_set_wait_limit.argtypes = [ctypes.c_uint64]
             lib.trellis_load_floor.restype = i32
             lib.trellis_load_floor.argtypes = [vp, vp, g, vp]
             lib.trellis_load_floor_rows.restype = i32
@@ -272,6 +275,11 @@ def prefill_plan(M: int, g: Geometry, sms: int = 0):
     n = load().trellis_prefill_plan(M, ctypes.byref(g.c()), sms, ctypes.byref(bn), buf)
     _check("trellis_prefill_plan", n if n < 0 else 0)
     return bn.value, [tuple(buf[3 * i:3 * i + 3]) for i in range(n)]
+
+
+def set_wait_limit(nanoseconds: int = 0) -> None:
+    """Diagnostic: limit of each bounded wait of the tensor-core kernel for later launches (0: the default)."""
+    _check("trellis_set_wait_limit", load().trellis_set_wait_limit(int(nanoseconds)))
 
 
 def device_error(reset: bool = False) -> int:

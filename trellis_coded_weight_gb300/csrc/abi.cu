@@ -263,6 +263,11 @@ int trellis_load_floor_rows(const uint32_t* codes, uint32_t* out, const trellis_
       trellis::launch_load_floor_rows(codes, out, g->k, g->rows, g->cols, static_cast<cudaStream_t>(stream)));
 }
 
+int trellis_set_wait_limit(uint64_t nanoseconds) {
+  trellis::set_wait_limit_ns(nanoseconds);
+  return TRELLIS_OK;
+}
+
 int trellis_device_error(int reset) {
   int st = device_ok();
   if (st) return st;

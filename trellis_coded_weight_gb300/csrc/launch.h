@@ -78,5 +78,7 @@ cudaError_t launch_load_floor_rows(const uint32_t* codes, uint32_t* out, int k, 
 
 // Device error word of the tensor-core kernels (bounded waits that gave up).
 int read_device_error(int reset);
+// Limit of each bounded wait of the tensor-core kernels for later launches (ns; 0: the 2 s default).
+void set_wait_limit_ns(uint64_t ns);
 
 }  // namespace trellis

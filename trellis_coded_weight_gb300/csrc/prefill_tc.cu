@@ -43,6 +43,7 @@
 // each tile's reduction and sums the partial accumulators through
 // distributed shared memory (epilogue, split reduction); with more, the full
 // waves run unsplit and the leftover tiles run split in a second launch.
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <cuda.h>
@@ -65,7 +66,12 @@ namespace {
 constexpr int kBM = 128;  // weight rows per tile (MMA M)
 constexpr int kProdWarp = 0, kMmaWarp = 1, kEpiWarp0 = 2, kEpiWarps = 4, kDecWarp0 = 6, kDecWarps = 16;
 constexpr int kThreads = 32 * (kDecWarp0 + kDecWarps);  // 704
-constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait: far beyond any legitimate wait
+constexpr uint64_t kWaitNs = 2000000000ull;  // default limit per wait: 2 s, far beyond any legitimate wait
+// Waits for work already issued (TMA copies in flight, committed MMAs) before a CTA exits after a failure
+// always use this limit: those operations finish by themselves, and the CTA must not leave before they do.
+constexpr uint64_t kDrainNs = 2000000000ull;
+// The limit given to launches (host side); a diagnostic setter changes it for tests of the error path.
+std::atomic<uint64_t> g_wait_ns{kWaitNs};
 
 
 struct PrefillParams {
@@ -80,6 +86,7 @@ struct PrefillParams {
   int tma_out;      // 1: out written by TMA tensor stores (nOut % 8 == 0)
   int S;            // axis 0: CTAs (a cluster) splitting each tile's reduction; 1 = no split
   int t0;           // first tile of this launch: it runs tiles t0 .. t0 + nTiles - 1
+  uint64_t wait_ns; // limit of each pipeline wait (%globaltimer ns); a wait that runs out sets the error word
 };
 
 constexpr int kMaxChunks = 16;  // 32-column chunks of the widest accumulator (BN = 512)
@@ -295,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int m0 = (t / p.nRT) * BN;
         for (int ks = 0; ks < kcnt; ++ks, ++g) {
           const int s = (int)(g % NS);
-          if (g >= NS && !tc::mbar_wait(empty + s, (uint32_t)((g / NS) & 1) ^ 1u, kWaitNs)) { *fail = 1; break; }
+          if (g >= NS && !tc::mbar_wait(empty + s, (uint32_t)((g / NS) & 1) ^ 1u, p.wait_ns)) { *fail = 1; break; }
           tc::mbar_arrive_expect_tx(full_b + s, (uint32_t)C_::BTile);
 #pragma unroll
           for (int h = 0; h < NH; ++h)
@@ -305,25 +312,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++issued;
         }
       }
-      if (*fail) {  // let copies already in flight land before the CTA exits
-        for (int64_t j = (issued > NS ? issued - NS : 0); j < issued; ++j)
-          tc::mbar_wait(full_b + j % NS, (uint32_t)((j / NS) & 1), kWaitNs);
-      }
+      // every copy issued has landed before the CTA exits (the MMA warp waited for all but the last NS of
+      // them; after a failure elsewhere it may not have waited for those)
+      for (int64_t j = (issued > NS ? issued - NS : 0); j < issued; ++j)
+        tc::mbar_wait(full_b + j % NS, (uint32_t)((j / NS) & 1), kDrainNs);
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       const uint32_t a0 = tc::smem_u32(a_tiles), b0 = tc::smem_u32(b_tiles);
-      int64_t g = 0;
+      int64_t g = 0, last = -1;  // last: the latest stage whose MMAs were committed
       for (int lt = 0; lt < n_local && !*fail; ++lt) {
         const int buf = lt % NACC, use = lt / NACC;
-        if (use >= 1 && !tc::mbar_wait(acc_empty + buf, (uint32_t)((use - 1) & 1), kWaitNs)) { *fail = 1; break; }
+        if (use >= 1 && !tc::mbar_wait(acc_empty + buf, (uint32_t)((use - 1) & 1), p.wait_ns)) { *fail = 1; break; }
         tc::fence_after_sync();
         const uint32_t d = tmem + (uint32_t)(buf * BN);
         bool ok = true;
         for (int ks = 0; ks < kcnt; ++ks, ++g) {
           const int s = (int)(g % NS);
           const uint32_t ph = (uint32_t)((g / NS) & 1);
-          if (!tc::mbar_wait(full_a + s, ph, kWaitNs) || !tc::mbar_wait(full_b + s, ph, kWaitNs)) { ok = false; break; }
+          if (!tc::mbar_wait(full_a + s, ph, p.wait_ns) || !tc::mbar_wait(full_b + s, ph, p.wait_ns)) { ok = false; break; }
           tc::fence_after_sync();
           const uint64_t ad = tc::desc_kmajor(a0 + s * C_::ATile, C_::SBO, C_::SwMode);
 #pragma unroll
@@ -334,10 +341,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc::mma_bf16(d + h * NMMA, ad + 2 * kk, bd + 2 * kk, kIdesc, (ks | kk) != 0 ? 1u : 0u);
           }
           tc::mma_commit(empty + s);
+          last = g;
         }
         if (!ok) { *fail = 1; break; }  // no commit without MMAs behind it
         tc::mma_commit(acc_full + buf);
       }
+      // the MMAs issued have finished (their last commit arrived) before this CTA frees its tensor memory
+      // and exits: normally the epilogue waited for them, but not if one of its waits ran out
+      if (last >= 0) tc::mbar_wait(empty + last % NS, (uint32_t)((last / NS) & 1), kDrainNs);
     }
   } else if (warp < kEpiWarp0 + kEpiWarps && split) {
     // ---------------- epilogue, split reduction (axis 0) ----------------
@@ -355,12 +366,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t row = rbase + lane;
     const int m0 = (t / p.nRT) * BN;
     constexpr int NCH = BN / 32;
-    bool ok = __all_sync(0xffffffffu, tc::mbar_wait(acc_full, 0u, kWaitNs));
+    bool ok = __all_sync(0xffffffffu, tc::mbar_wait(acc_full, 0u, p.wait_ns));
     tc::fence_after_sync();
     for (int i = 0; i < NCH && ok; ++i) {
       const int b = i & 1, owner = i % S;
       float* mine = red[b];
-      if (i >= 2 && !(ok = __all_sync(0xffffffffu, tc::mbar_wait_cluster(done + (i - 2), 0u, kWaitNs)))) break;
+      if (i >= 2 && !(ok = __all_sync(0xffffffffu, tc::mbar_wait_cluster(done + (i - 2), 0u, p.wait_ns)))) break;
       uint32_t v[32];
       tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * sp) << 16) + (uint32_t)(32 * i), v);
       tc::tmem_ld_wait();
@@ -370,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) tc::mbar_arrive_cluster(ready + i, (uint32_t)owner);
       if (rank == owner) {
-        if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait_cluster(ready + i, 0u, kWaitNs)))) break;
+        if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait_cluster(ready + i, 0u, p.wait_ns)))) break;
         float acc[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) acc[j] = 0.f;
@@ -395,9 +406,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int r = 0; r < S; ++r) tc::mbar_arrive_cluster(done + i, (uint32_t)r);
       }
     }
-    // the owners of this CTA's last two chunks have read its buffers (waited even after a failure)
+    // the owners of this CTA's last two chunks have read its buffers (waited even after a failure; the
+    // cluster barrier before exit covers an owner that is still reading when this wait runs out)
     for (int i = (NCH > 2 ? NCH - 2 : 0); i < NCH; ++i)
-      if (!__all_sync(0xffffffffu, tc::mbar_wait_cluster(done + i, 0u, kWaitNs))) ok = false;
+      if (!__all_sync(0xffffffffu, tc::mbar_wait_cluster(done + i, 0u, p.wait_ns))) ok = false;
     if (!ok) *fail = 1;
   } else if (warp < kEpiWarp0 + kEpiWarps) {
     // ---------------- epilogue ----------------
@@ -405,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int ec = 0;               // staging buffers alternate per stored chunk
     for (int lt = 0; lt < n_local; ++lt) {
       const int buf = lt % NACC, use = lt / NACC;
-      const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(acc_full + buf, (uint32_t)(use & 1), kWaitNs));
+      const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(acc_full + buf, (uint32_t)(use & 1), p.wait_ns));
       tc::fence_after_sync();
       if (!ok) { *fail = 1; break; }
       const int t = p.t0 + cid + lt * G;
@@ -484,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         // warp-uniform outcome: the transposing store below is a whole-warp instruction
-        if (g >= NS && !__all_sync(0xffffffffu, tc::mbar_wait(empty + s, (uint32_t)((g / NS) & 1) ^ 1u, kWaitNs))) {
+        if (g >= NS && !__all_sync(0xffffffffu, tc::mbar_wait(empty + s, (uint32_t)((g / NS) & 1) ^ 1u, p.wait_ns))) {
           *fail = 1;
           break;
         }
@@ -554,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // one stage: decode run qh (of the half block) into slot g % NS
       auto stage = [&](const RunWords<K>& rw, int g) -> bool {
         const int s = g % NS;
-        if (g >= NS && !tc::mbar_wait(empty + s, (uint32_t)((g / NS) & 1) ^ 1u, kWaitNs)) return false;
+        if (g >= NS && !tc::mbar_wait(empty + s, (uint32_t)((g / NS) & 1) ^ 1u, p.wait_ns)) return false;
         decode_run_to_tile<K, L>(rw, a_tiles + (size_t)s * C_::ATile + rl * RowBytes, sw, 4 * h);
         tc::fence_proxy_async_smem();
         __syncwarp();
@@ -617,6 +629,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc::fence_before_sync();
   __syncthreads();
+  // split: no CTA of the cluster leaves while a peer may still read its chunk buffers or arrive on its
+  // barriers (every wait is bounded, so every CTA gets here)
+  if (split) tc::cluster_sync_all();
   if (threadIdx.x == 0 && *fail) report(1);
   if (warp == kMmaWarp) {
     tc::fence_after_sync();
@@ -800,8 +815,12 @@ cudaError_t launch_gemm_prefill(const uint32_t* codes, const uint16_t* scales, c
   p.R = rows; p.C = cols; p.M = M; p.nb = (int)(cols / kT);
   p.nOut = axis == 1 ? rows : cols;
   p.Kd = axis == 1 ? cols : rows;
+  p.wait_ns = g_wait_ns.load();
   return axis == 1 ? prefill_axis<1>(p, x, k, L, st) : prefill_axis<0>(p, x, k, L, st);
 }
+
+// Limit of each pipeline wait of the tensor-core kernels (ns); 0 restores the default.
+void set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns ? ns : kWaitNs); }
 
 // Read (and optionally clear) the device error word.
 int read_device_error(int reset) {

@@ -51,11 +51,36 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, with the thread suspended at most about hint_ns while the phase is incomplete.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Limits below this are test settings: each try suspends at most the limit and the deadline is checked
+// after every try, so the wait runs out within about twice the limit.
+constexpr uint64_t kShortWaitNs = 1000000ull;
+
 // Wait for the phase of the given parity; false once timeout_ns (of
-// %globaltimer) have passed since the first unsuccessful try.
+// %globaltimer) have passed since the first unsuccessful try.  Each try may
+// suspend the thread until the phase completes (a hardware time limit ends
+// the suspension), so the deadline is checked every 64 tries.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t deadline = globaltimer() + timeout_ns;
+  if (timeout_ns < kShortWaitNs) {
+    for (;;) {
+      if (mbar_try_wait_hint(bar, parity, (uint32_t)timeout_ns)) return true;
+      if (globaltimer() > deadline) return false;
+    }
+  }
   for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 63u && globaltimer() > deadline) return false;
@@ -103,10 +128,28 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
   return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_try_wait_cluster_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // As mbar_wait, with acquire at cluster scope (arrivals came from other CTAs).
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
   const uint64_t deadline = globaltimer() + timeout_ns;
+  if (timeout_ns < kShortWaitNs) {
+    for (;;) {
+      if (mbar_try_wait_cluster_hint(bar, parity, (uint32_t)timeout_ns)) return true;
+      if (globaltimer() > deadline) return false;
+    }
+  }
   for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     if ((i & 63u) == 63u && globaltimer() > deadline) return false;
