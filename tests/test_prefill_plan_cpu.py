@@ -9,7 +9,8 @@ The plan is the host arithmetic trellis_gemm_prefill launches by:
 
 These tests pin the policy and the invariants every plan must keep: each
 tile in exactly one launch, clusters that fit the SMs, and cluster sizes
-within the portable limit, the reduction's stage count and the per-BN cap.
+within the portable limit (8, whose reduction slots fit in the stage ring) and
+the reduction's stage count.
 """
 import ctypes
 
@@ -59,18 +60,19 @@ def test_axis0_pages_shapes():
     assert tb.prefill_plan(64, g, 152) == (64, [(0, 40, 3)])
     assert tb.prefill_plan(512, g, 152) == (512, [(0, 40, 3)])
     assert tb.prefill_plan(1024, g, 152) == (512, [(0, 80, 1)])   # 80 tiles: no room for 2 CTAs each
-    # 160 tiles: the full wave unsplit, then the 8 leftover tiles split (4 CTAs, the BN = 512 cap)
-    assert tb.prefill_plan(2048, g, 152) == (512, [(0, 152, 1), (152, 8, 4)])
-    assert tb.prefill_plan(2048, g, 148) == (512, [(0, 148, 1), (148, 12, 4)])
+    # 160 tiles: the full wave unsplit, then the 8 leftover tiles split over 8-CTA clusters
+    assert tb.prefill_plan(2048, g, 152) == (512, [(0, 152, 1), (152, 8, 8)])
+    assert tb.prefill_plan(2048, g, 148) == (512, [(0, 148, 1), (148, 12, 8)])
     assert tb.prefill_plan(2048, g, 160) == (512, [(0, 160, 1)])  # whole waves: nothing left over
 
 
 def test_split_caps():
-    # BN = 256: at most 5 CTAs per tile; BN <= 128: the portable cluster size 8; short reductions: nk
+    # every BN: at most the portable cluster size 8; short reductions: at most nk
     g = tb.Geometry(3, 16, 256, 0, 17408, 1024)                   # 8 feature tiles
-    assert tb.prefill_plan(200, g, 152)[1] == [(0, 8, 5)]
+    assert tb.prefill_plan(200, g, 152)[1] == [(0, 8, 8)]
     assert tb.prefill_plan(100, g, 152)[1] == [(0, 8, 8)]
-    assert tb.prefill_plan(600, g, 152)[1] == [(0, 16, 4)]
+    assert tb.prefill_plan(600, g, 152)[1] == [(0, 16, 8)]
+    assert tb.prefill_plan(600, g, 100)[1] == [(0, 16, 6)]        # 16 tiles x 6 CTAs fill 96 of 100 SMs
     short = tb.Geometry(3, 16, 256, 0, 96, 5376)                  # 96 rows: 3 stages of 32 at BN = 512
     assert tb.prefill_plan(1600, short, 152) == (512, [(0, 152, 1), (152, 16, 3)])
     assert tb.prefill_plan(8, tb.Geometry(2, 16, 256, 0, 64, 5120), 152)[1] == [(0, 40, 1)]  # 1 stage of 64
@@ -97,7 +99,6 @@ def test_plan_invariants(sms, axis):
                     assert S == 1
                 if S > 1:
                     assert n * S <= sms, "the clusters of a split launch run at once"
-                    assert S <= (4 if bn == 512 else 5 if bn == 256 else 8)
 
 
 def test_plan_argument_errors():

@@ -90,6 +90,11 @@ struct PrefillParams {
 };
 
 constexpr int kMaxChunks = 16;  // 32-column chunks of the widest accumulator (BN = 512)
+// Split reduction slots (in the owner's stage ring): 128 rows x 32 fp32, rows padded to 144 bytes so that
+// the owner's 16-byte row reads of a warp spread over the banks.
+constexpr int kSlotRow = 144;
+constexpr int kSlotBytes = kBM * kSlotRow;
+constexpr int kMaxSplit = 8;  // the plan's largest cluster
 
 // AX0: axis-0 kernel (reserves the split reduction's chunk buffer).
 template <int BN, int BK, bool AX0 = false>
@@ -101,10 +106,7 @@ struct Cfg {
   static constexpr int BTile = BN * BK * 2;
   static constexpr int Stage = ATile + BTile;
   static constexpr int EpiBytes = kEpiWarps * 2 * 32 * 32 * 2;  // per warp: two 32x32 bf16 sub-tiles
-  // axis 0 split: two fp32 [32][128] chunk buffers, the first in the (then unused) bf16 epilogue staging
-  static constexpr int RedBytes = AX0 ? 32 * kBM * 4 : 0;
-  static_assert(EpiBytes == 32 * kBM * 4, "the epilogue staging holds one fp32 chunk");
-  static constexpr int NS0 = (220 * 1024 - EpiBytes - RedBytes) / Stage;
+  static constexpr int NS0 = (220 * 1024 - EpiBytes) / Stage;
   static constexpr int NS = NS0 > 8 ? 8 : NS0;         // ring stages
   static constexpr int TmemCols = NACC * BN < 32 ? 32 : NACC * BN;
   static constexpr int RunsPerRow = BK / 32;            // runs of 32 positions per row and stage
@@ -113,7 +115,9 @@ struct Cfg {
   static constexpr uint32_t SBO = 8u * BK * 2u;         // bytes between 8-row groups
   static constexpr uint32_t SwMode = BK == 64 ? 2u : 4u;  // descriptor swizzle: 128B or 64B
   static constexpr CUtensorMapSwizzle TmaSw = BK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-  static constexpr size_t Smem = 1024 + (size_t)NS * Stage + EpiBytes + RedBytes + 1024;
+  static constexpr size_t Smem = 1024 + (size_t)NS * Stage + EpiBytes + 1024;
+  // axis 0 split: the slots of every sender of the largest cluster fit in the idle stage ring
+  static_assert(!AX0 || kMaxSplit * kSlotBytes <= NS * Stage, "split reduction slots exceed the stage ring");
   static_assert(BK == 64 || BK == 32, "stage width");
   static_assert(NS >= 2, "ring too small");
   // a decoder group's consecutive stages are Groups apart: within one lap of the ring, so that an
@@ -239,9 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* a_tiles = smem;                                // NS x ATile
   uint8_t* b_tiles = smem + (size_t)NS * C_::ATile;       // NS x BTile
   uint8_t* epi_stage = smem + (size_t)NS * C_::Stage;     // kEpiWarps x 2 x [32 tokens][32 rows] bf16
-  // axis 0 split: chunk buffer 0 is the epilogue staging, buffer 1 follows it; [32][128] fp32 each
-  float* red[2] = {reinterpret_cast<float*>(epi_stage), reinterpret_cast<float*>(epi_stage + C_::EpiBytes)};
-  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_stage + C_::EpiBytes + C_::RedBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_stage + C_::EpiBytes);
   uint64_t* full_a = bars;                 // decoder group -> MMA
   uint64_t* full_b = bars + NS;            // TMA -> MMA (1 arrival + tx bytes)
   uint64_t* empty = bars + 2 * NS;         // MMA commit -> producer and decoders
@@ -249,8 +251,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_empty = bars + 3 * NS + 2; // [NACC] epilogue warps -> MMA
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * NS + 4);
   volatile int* fail = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  uint64_t* ready = bars + 3 * NS + 5;              // [kMaxChunks] split: partials of a chunk -> its owner
-  uint64_t* done = bars + 3 * NS + 5 + kMaxChunks;  // [kMaxChunks] split: the owner has read a chunk
+  uint64_t* ready = bars + 3 * NS + 5;                  // [kMaxChunks] split: partials of a round -> its owner
+  uint64_t* done = bars + 3 * NS + 5 + kMaxChunks;      // [kMaxChunks] split: the owners have read a round
+  uint64_t* ringfree = bars + 3 * NS + 5 + 2 * kMaxChunks;  // split: every other CTA's MMAs are done
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Without a split a CTA walks tiles cid, cid + G, ... over all nk stages.  With a split (axis 0), the S
@@ -275,11 +278,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(acc_full + b, 1);
       tc::mbar_init(acc_empty + b, kEpiWarps);
     }
-    if (split)
-      for (int i = 0; i < kMaxChunks; ++i) {
-        tc::mbar_init(ready + i, kEpiWarps * S);
-        tc::mbar_init(done + i, kEpiWarps);
+    if (split) {
+      // ready[rd]: the owner's expect_tx arrival (plus the senders' bytes); done[rd]: one arrival per
+      // epilogue warp of every owner of round rd this CTA sent to; ringfree: one from every other CTA
+      constexpr int NCH = BN / 32;
+      for (int rd = 0; rd < kMaxChunks; ++rd) {
+        const int nown = NCH - rd * S < S ? NCH - rd * S : S;
+        const int others = nown > 0 ? nown - (rank < nown ? 1 : 0) : 0;
+        tc::mbar_init(ready + rd, 1);
+        tc::mbar_init(done + rd, others > 0 ? kEpiWarps * others : 1);
       }
+      tc::mbar_init(ringfree, S - 1);
+    }
     *fail = 0;
     tc::fence_mbar_init();
   }
@@ -352,64 +362,108 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < kEpiWarp0 + kEpiWarps && split) {
     // ---------------- epilogue, split reduction (axis 0) ----------------
-    // The cluster's S CTAs hold partial accumulators of one tile.  Chunk i
-    // (32 columns) is summed by CTA i % S: every CTA writes its partial of
-    // the chunk, fp32 [32 columns][128 rows], into its buffer i % 2 and
-    // arrives on the owner's ready[i]; the owner reads the S partials through
-    // distributed shared memory in rank order, stores bf16 and arrives on
-    // every CTA's done[i], which frees that buffer for chunk i + 2.  All
-    // barriers are single-use; no CTA leaves before the owners of its last
-    // two chunks are done with its buffers.
+    // The cluster's S CTAs hold partial accumulators of one tile.  The tile's
+    // 32-column chunks go round by round to owners: in round rd, chunk
+    // rd*S + q belongs to CTA q.  Every CTA reads each chunk of the round
+    // from tensor memory; a non-owner pushes its fp32 rows with st.async
+    // into slot [its rank] of the owner's stage ring (idle once the owner's
+    // MMAs are done), completing bytes on the owner's ready[rd]; the owner
+    // sums the S partials in rank order (its own from registers), stores
+    // bf16 and tells every sender (done[rd]) that the slots are free again.
+    // No CTA writes into another's ring before that CTA's MMAs are done
+    // (ringfree).  All barriers are single-use and every wait is bounded;
+    // after a failure an owner still waits (with the drain limit) for the
+    // bytes it was promised, so nothing lands in a CTA that has left.
     const int sp = warp & 3;
     const int t = p.t0 + cid;
-    const int64_t rbase = (int64_t)(t % p.nRT) * kBM + 32 * sp;
-    const int64_t row = rbase + lane;
+    const int64_t row = (int64_t)(t % p.nRT) * kBM + 32 * sp + lane;
     const int m0 = (t / p.nRT) * BN;
     constexpr int NCH = BN / 32;
-    bool ok = __all_sync(0xffffffffu, tc::mbar_wait(acc_full, 0u, p.wait_ns));
+    constexpr uint32_t kRoundBytes = kBM * 32 * 4;  // one sender's rows of one chunk
+    const int rounds = (NCH + S - 1) / S;
+    auto owners = [&](int rd) { return NCH - rd * S < S ? NCH - rd * S : S; };  // ranks 0 .. owners-1
+    // the four epilogue warps take every branch together (named barrier 1, an AND over their waits)
+    auto all_ok = [&](bool v) { return tc::bar_and(v, 1, kEpiWarps * 32); };
+    int invited = -1;     // a round whose partials the others may be sending to this owner, not yet received
+    int registered = -1;  // the last round whose bytes this owner has announced on ready[]
+    bool ok = all_ok(tc::mbar_wait(acc_full, 0u, p.wait_ns));
     tc::fence_after_sync();
-    for (int i = 0; i < NCH && ok; ++i) {
-      const int b = i & 1, owner = i % S;
-      float* mine = red[b];
-      if (i >= 2 && !(ok = __all_sync(0xffffffffu, tc::mbar_wait_cluster(done + (i - 2), 0u, p.wait_ns)))) break;
-      uint32_t v[32];
-      tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * sp) << 16) + (uint32_t)(32 * i), v);
-      tc::tmem_ld_wait();
+    if (ok) {
+      if (sp == 0 && lane == 0)
+        for (int r = 0; r < S; ++r)
+          if (r != rank) tc::mbar_arrive_cluster(ringfree, (uint32_t)r);
+      if (rank < owners(0)) invited = 0;
+      ok = all_ok(tc::mbar_wait_cluster(ringfree, 0u, p.wait_ns));
+    }
+    for (int rd = 0; rd < rounds && ok; ++rd) {
+      // every round before the last has S owners: all of them got this CTA's partials of that round
+      if (rd > 0 && !(ok = all_ok(tc::mbar_wait_cluster(done + rd - 1, 0u, p.wait_ns)))) break;
+      const bool owner = rank < owners(rd);
+      if (owner) {
+        if (sp == 0 && lane == 0) tc::mbar_arrive_expect_tx(ready + rd, (uint32_t)(S - 1) * kRoundBytes);
+        registered = rd;
+      }
+      for (int q = 0; q < owners(rd); ++q) {  // this CTA's partials of the other owners' chunks
+        if (q == rank) continue;
+        uint32_t v[32];
+        tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * sp) << 16) + (uint32_t)(32 * (rd * S + q)), v);
+        tc::tmem_ld_wait();
+        const uint32_t dst =
+            tc::mapa_shared(a_tiles + (size_t)rank * kSlotBytes + (32 * sp + lane) * kSlotRow, (uint32_t)q);
+        const uint32_t bar = tc::mapa_shared(ready + rd, (uint32_t)q);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) mine[j * kBM + 32 * sp + lane] = __uint_as_float(v[j]);
-      tc::fence_acq_rel_cluster();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive_cluster(ready + i, (uint32_t)owner);
-      if (rank == owner) {
-        if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait_cluster(ready + i, 0u, p.wait_ns)))) break;
-        float acc[32];
+        for (int k4 = 0; k4 < 8; ++k4)
+          tc::st_async_v4(dst + 16 * k4, __uint_as_float(v[4 * k4]), __uint_as_float(v[4 * k4 + 1]),
+                          __uint_as_float(v[4 * k4 + 2]), __uint_as_float(v[4 * k4 + 3]), bar);
+      }
+      if (!owner) continue;
+      if (!(ok = all_ok(tc::mbar_wait_cluster(ready + rd, 0u, p.wait_ns)))) break;
+      invited = -1;
+      float acc[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) acc[j] = 0.f;
-        for (int r = 0; r < S; ++r) {
+      for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+      for (int r = 0; r < S; ++r) {  // rank order: the sum does not depend on arrival order
+        if (r == rank) {             // this CTA's own partial, straight from tensor memory
+          uint32_t v[32];
+          tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * sp) << 16) + (uint32_t)(32 * (rd * S + rank)), v);
+          tc::tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) acc[j] += tc::ld_dsmem_f32(mine + j * kBM + 32 * sp + lane, (uint32_t)r);
-        }
-        if (row < p.nOut) {
+          for (int j = 0; j < 32; ++j) acc[j] += __uint_as_float(v[j]);
+        } else {
+          const float4* src =
+              reinterpret_cast<const float4*>(a_tiles + (size_t)r * kSlotBytes + (32 * sp + lane) * kSlotRow);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int m = m0 + 32 * i + j;
-            if (m < p.M) {
-              uint16_t o;
-              asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(o) : "f"(acc[j]));
-              p.out[(int64_t)m * p.nOut + row] = o;
-            }
+          for (int k4 = 0; k4 < 8; ++k4) {
+            const float4 f = src[k4];
+            acc[4 * k4] += f.x; acc[4 * k4 + 1] += f.y; acc[4 * k4 + 2] += f.z; acc[4 * k4 + 3] += f.w;
           }
         }
-        tc::fence_acq_rel_cluster();
-        __syncwarp();
-        if (lane == 0)
-          for (int r = 0; r < S; ++r) tc::mbar_arrive_cluster(done + i, (uint32_t)r);
       }
+      if (row < p.nOut) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int m = m0 + 32 * (rd * S + rank) + j;
+          if (m < p.M) {
+            uint16_t o;
+            asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(o) : "f"(acc[j]));
+            p.out[(int64_t)m * p.nOut + row] = o;
+          }
+        }
+      }
+      tc::fence_acq_rel_cluster();  // the slot reads above complete before the senders may refill them
+      __syncwarp();
+      if (lane == 0)
+        for (int r = 0; r < S; ++r)
+          if (r != rank) tc::mbar_arrive_cluster(done + rd, (uint32_t)r);
+      if (rd + 1 < rounds && rank < owners(rd + 1)) invited = rd + 1;
     }
-    // the owners of this CTA's last two chunks have read its buffers (waited even after a failure; the
-    // cluster barrier before exit covers an owner that is still reading when this wait runs out)
-    for (int i = (NCH > 2 ? NCH - 2 : 0); i < NCH; ++i)
-      if (!__all_sync(0xffffffffu, tc::mbar_wait_cluster(done + i, 0u, p.wait_ns))) ok = false;
+    // after a failure: partials the others may be sending this owner land before the CTA may leave (the
+    // wait ends at once if they arrived, after the drain limit if no sender got that far)
+    if (invited >= 0) {
+      if (registered != invited && sp == 0 && lane == 0)
+        tc::mbar_arrive_expect_tx(ready + invited, (uint32_t)(S - 1) * kRoundBytes);
+      tc::mbar_wait_cluster(ready + invited, 0u, kDrainNs);
+    }
     if (!ok) *fail = 1;
   } else if (warp < kEpiWarp0 + kEpiWarps) {
     // ---------------- epilogue ----------------
@@ -779,9 +833,9 @@ cudaError_t prefill_axis(const PrefillParams& p, const uint16_t* x, int k, int L
 //   - when they leave SMs idle, a cluster of S CTAs splits each tile's reduction (S * tiles <= SMs);
 //   - when they overrun whole waves, the full waves run unsplit and the tiles left over run split in a
 //     second launch, instead of as a nearly empty wave.
-// The split reduction runs BN/32 chunk rounds whose cost grows with S (measured at BN = 512: about 20 us
-// per CTA of the cluster against 300 us for a whole tile), so S stops at round(sqrt(240 / chunks)): 4 for
-// BN = 512, 5 for BN = 256, 8 (the portable cluster size) below; and at the reduction's stage count.
+// The split reduction pushes each CTA's partial rows into the owners' shared memory with st.async, a few
+// microseconds per tile whatever S is, so S goes up to the portable cluster size 8 (whose senders' slots
+// fit in the idle stage ring) and at most the reduction's stage count.
 int device_sm_count() { return sm_count(); }
 
 int prefill_plan(int M, int axis, int64_t nOut, int64_t Kd, int sms, int* tokens_per_tile, PrefillLaunch* launches) {
@@ -789,7 +843,7 @@ int prefill_plan(int M, int axis, int64_t nOut, int64_t Kd, int sms, int* tokens
   const int BK = BN == 512 ? 32 : 64;
   const int nk = (int)((Kd + BK - 1) / BK);
   const int nTiles = (int)((nOut + kBM - 1) / kBM) * ((M + BN - 1) / BN);
-  const int cap = BN >= 512 ? 4 : (BN >= 256 ? 5 : 8);
+  const int cap = kMaxSplit;
   if (sms < 1) sms = 1;
   auto split_of = [&](int count) {
     int S = sms / count;

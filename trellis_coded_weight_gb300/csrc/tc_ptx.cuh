@@ -101,6 +101,21 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// AND of v over the `count` threads (whole warps) that take part in named barrier `id`; every one of them
+// must execute it.  Used where a group of warps must take the same branch after waits that each may run out.
+__device__ __forceinline__ bool bar_and(bool v, int id, int count) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred q, o;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "barrier.red.and.pred o, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, o;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
 
 // Shared-memory address of the same object in CTA `rank` of the cluster.
@@ -154,6 +169,14 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
     if (mbar_try_wait_cluster(bar, parity)) return true;
     if ((i & 63u) == 63u && globaltimer() > deadline) return false;
   }
+}
+
+// Four fp32 into the shared memory of another CTA of the cluster (addr and bar already mapped with
+// mapa_shared), completing 16 transaction bytes on that CTA's mbarrier when they land.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, float c, float d, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+               ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d), "r"(bar)
+               : "memory");
 }
 
 // fp32 at the same shared-memory offset in CTA `rank` of the cluster.
