@@ -294,39 +294,34 @@ def run_gpu(args):
 
 
 def run_e2e(args, torch, tdist, tb, dev, stream, bufs, scales, geoms, xs, rot, world, sync_all):
-    """The headline through the C ABI with host buffers: every launch copies its x in from pinned host memory
-    and its output back.  The copies run on their own streams so that they overlap the neighbouring launches:
-    the x of each launch goes in ahead on the h2d stream, each output goes out on the d2h stream while the next
-    launch runs.  Each (k, M) slot has its own device buffers; events order the reuse of a slot across steps."""
+    """The headline through the C ABI with host buffers: each launch is one trellis_matvec_axis1_host call, which
+    queues the copy of its x from pinned host memory, the matvec and the copy of its output back to pinned host
+    memory, in order on the launching stream.  Each (k, M) slot has its own host and device buffers; the
+    arguments are prepared once (pointers, geometry, stream), as for the device-timed headline."""
+    lib = tb.load()
     slots = [(k, M) for k in KS for M in MS]
     x_host = {M: xs[M].cpu().pin_memory() for M in MS}
     o_host = {s: torch.empty((s[1], R), dtype=torch.bfloat16).pin_memory() for s in slots}
     x_dev = {s: torch.empty_like(xs[s[1]]) for s in slots}
     o_dev = {s: torch.empty((s[1], R), dtype=torch.bfloat16, device=dev) for s in slots}
-    h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev = {s: {n: torch.cuda.Event() for n in ("h2d", "kern", "d2h")} for s in slots}
-    for s in slots:  # recorded once so that the first waits are satisfied
-        for e in ev[s].values():
-            e.record(stream)
+    sptr = stream.cuda_stream
+    cargs = {}
+    for (k, M) in slots:  # the binding's checks once, then the prepared C arguments per code buffer
+        tb.matvec_axis1_host(bufs[k][0], scales[k], x_host[M], geoms[k], o_host[(k, M)], x_dev[(k, M)],
+                             o_dev[(k, M)])
+        for i, b in enumerate(bufs[k]):
+            cargs[(k, M, i)] = (b.data_ptr(), scales[k].data_ptr(), x_host[M].data_ptr(), o_host[(k, M)].data_ptr(),
+                                M, ctypes.byref(geoms[k].c()), x_dev[(k, M)].data_ptr(), o_dev[(k, M)].data_ptr(),
+                                sptr)
+    fn = lib.trellis_matvec_axis1_host
 
     def e2e_step():
-        with torch.cuda.stream(h2d_stream):
-            for s in slots:
-                h2d_stream.wait_event(ev[s]["kern"])  # the slot's previous launch has read its x
-                x_dev[s].copy_(x_host[s[1]], non_blocking=True)
-                ev[s]["h2d"].record(h2d_stream)
-        for s in slots:
-            k, M = s
-            stream.wait_event(ev[s]["h2d"])
-            stream.wait_event(ev[s]["d2h"])  # the slot's previous output has been read out
+        for (k, M) in slots:
             i = rot[k]
             rot[k] = (i + 1) % len(bufs[k])
-            tb.matvec_axis1(bufs[k][i], scales[k], x_dev[s], geoms[k], o_dev[s])
-            ev[s]["kern"].record(stream)
-            with torch.cuda.stream(d2h_stream):
-                d2h_stream.wait_event(ev[s]["kern"])
-                o_host[s].copy_(o_dev[s], non_blocking=True)
-                ev[s]["d2h"].record(d2h_stream)
+            st = fn(*cargs[(k, M, i)])
+            if st:
+                raise RuntimeError(f"trellis_matvec_axis1_host returned {st}")
 
     for _ in range(args.warmup):
         e2e_step()
@@ -335,8 +330,7 @@ def run_e2e(args, torch, tdist, tb, dev, stream, bufs, scales, geoms, xs, rot, w
     a.record(stream)
     for _ in range(args.steps):
         e2e_step()
-    stream.wait_stream(d2h_stream)  # the timed region ends when the last output is back on the host
-    b.record(stream)
+    b.record(stream)  # after the last output's copy to the host
     sync_all()
     e2e_ms = a.elapsed_time(b)
     if world > 1:
@@ -346,7 +340,8 @@ def run_e2e(args, torch, tdist, tb, dev, stream, bufs, scales, geoms, xs, rot, w
     step_bytes = sum(packed_bytes(k) for k in KS for M in MS)
     return {"value": world * step_bytes * args.steps / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": sum(M * C * 2 for k in KS for M in MS),
-            "d2h_bytes_per_step": sum(M * R * 2 for k in KS for M in MS)}
+            "d2h_bytes_per_step": sum(M * R * 2 for k in KS for M in MS),
+            "call": "trellis_matvec_axis1_host (one C call per launch: x in, matvec, out back, on one stream)"}
 
 
 def run_rows(torch, tb, inputs, dev, timer, l2, bufs, scales, geoms):

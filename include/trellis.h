@@ -114,6 +114,29 @@ int trellis_matvec_axis1(const uint32_t *codes, const uint16_t *scales, const ui
                          uint16_t *out, int M, const trellis_geom_t *g, trellis_stream_t stream);
 
 /*
+ * trellis_matvec_axis1_host -- trellis_matvec_axis1 with x and out in host
+ * memory: one call queues, in order on `stream`, the copy of x_host
+ * [M][cols] bf16 into the caller's device buffer x_dev, the matvec into the
+ * caller's device buffer out_dev [M][rows], and the copy of out_dev into
+ * out_host.  It returns once they are queued; out_host holds the result when
+ * the stream has reached that point (synchronize the stream or an event
+ * recorded after the call).  The pages' decode call does the same for one
+ * token: its input arrives from the host and its output goes back.
+ *   x_host, out_host: host memory, no alignment rule; pinned memory
+ *   (cudaHostAlloc / cudaHostRegister) keeps the copies asynchronous, pageable
+ *   memory is copied through a driver staging buffer and the call may block.
+ *   x_dev, out_dev: device memory, 16-byte aligned, owned by the caller; they
+ *   must not be in use by other work until the stream has passed the call.
+ *   codes, scales, M, g: as for trellis_matvec_axis1.
+ * Errors: as for trellis_matvec_axis1 (TRELLIS_ENULL also for a NULL host or
+ * staging pointer, TRELLIS_EALIGN for a staging buffer); TRELLIS_ECUDA if a
+ * copy or the launch could not be queued.
+ */
+int trellis_matvec_axis1_host(const uint32_t *codes, const uint16_t *scales, const uint16_t *x_host,
+                              uint16_t *out_host, int M, const trellis_geom_t *g, uint16_t *x_dev,
+                              uint16_t *out_dev, trellis_stream_t stream);
+
+/*
  * trellis_matvec_axis0 -- decode-fused matvec for M = 1..4 input rows over
  * an axis-0 matrix, i.e. a stored W^T ("trellis-linear.ts": the scatter path
  * of TrellisLinear.forward, SCATTER_SOURCE and its partial fold;

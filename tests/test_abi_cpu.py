@@ -89,11 +89,26 @@ def test_errors_before_launch(lib):
     assert lib.trellis_matvec_axis0(A, A, A, A, 4, ctypes.byref(g), A, need, None) == -4
 
 
+def test_host_buffer_matvec_errors_before_any_copy(lib):
+    g = G()
+    H = 12345  # host pointers carry no alignment rule
+    f = lib.trellis_matvec_axis1_host
+    assert f(A, A, H, H, 1, None, A, A, None) == -7
+    assert f(A, A, H, H, 1, ctypes.byref(G(axis=0)), A, A, None) == -4
+    assert f(A, A, H, H, 5, ctypes.byref(g), A, A, None) == -2
+    assert f(A, A, None, H, 1, ctypes.byref(g), A, A, None) == -7
+    assert f(A, A, H, None, 1, ctypes.byref(g), A, A, None) == -7
+    assert f(A, A, H, H, 1, ctypes.byref(g), None, A, None) == -7
+    assert f(A, A, H, H, 1, ctypes.byref(g), A + 2, A, None) == -3
+    assert f(A, A, H, H, 1, ctypes.byref(g), A, A + 8, None) == -3
+
+
 def test_no_usable_device_without_gpu(lib):
     import torch
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert lib.trellis_matvec_axis1(A, A, A, A, 1, ctypes.byref(G()), None) == -8
+    assert lib.trellis_matvec_axis1_host(A, A, 7, 7, 1, ctypes.byref(G()), A, A, None) == -8
 
 
 def test_workspace_grows_with_M(lib):

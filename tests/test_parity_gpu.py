@@ -81,6 +81,29 @@ def test_matvec_axis1_config_smoke_shape(oracle_mod):
     check_band(oracle_mod, bf16_bits(out), ref, ab, "axis1 512x2048")
 
 
+@pytest.mark.parametrize("M", [1, 4])
+@pytest.mark.parametrize("pinned", [True, False])
+def test_matvec_axis1_host_buffers(oracle_mod, M, pinned):
+    """The host-buffer call: x from host memory, out back to host memory, in one call; the same bits as the
+    device call and within the oracle's band."""
+    rows, cols, k = 300, 1280, 3
+    codes, scales, x = inputs.make_linear(rows, cols, k, M, seed_codes=91, seed_x=92 + M)
+    g = tb.Geometry(k, L, T, 1, rows, cols)
+    dc, ds = to_dev_u32(codes), to_dev_f16(scales)
+    x_host = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16)
+    out_host = torch.full((M, rows), -1.0, dtype=torch.bfloat16)
+    if pinned:
+        x_host, out_host = x_host.pin_memory(), out_host.pin_memory()
+    x_dev = torch.empty((M, cols), dtype=torch.bfloat16, device="cuda")
+    out_dev = torch.empty((M, rows), dtype=torch.bfloat16, device="cuda")
+    tb.matvec_axis1_host(dc, ds, x_host, g, out_host, x_dev, out_dev)
+    torch.cuda.current_stream().synchronize()
+    dev = tb.matvec_axis1(dc, ds, to_dev_bf16(x), g)
+    assert torch.equal(out_host.view(torch.int16), dev.cpu().view(torch.int16))
+    ref, ab = oracle_mod.matvec_axis1(codes, scales, x, k, L, T)
+    check_band(oracle_mod, bf16_bits(out_host), ref, ab, f"axis1 host buffers M={M}")
+
+
 @pytest.mark.parametrize("k", [2, 3, 4])
 def test_matvec_axis1_full_size_sampled(oracle_mod, k):
     rows, cols, M = 17408, 5120, 4
@@ -222,6 +245,41 @@ def test_matvec_axis0_full_size_sampled(oracle_mod, k):
         out = bf16_bits(tb.matvec_axis0(dc, ds, to_dev_bf16(x[:m]), g, ws))
         ref, ab = oracle_mod.matvec_axis0(codes, scales, x[:m], k, L, T, cols=idx)
         check_band(oracle_mod, out[:, idx], ref, ab, f"axis0 full k={k} M={m}")
+
+
+@pytest.mark.parametrize("k", [2, 3, 4])
+def test_matvec_axis0_L12(oracle_mod, k):
+    rows, cols, M = 333, 768, 3
+    codes, scales, x = inputs.make_linear(rows, cols, k, M, seed_codes=61 + k, seed_x=62, sigma=0.5, x_len=rows)
+    g = tb.Geometry(k, 12, T, 0, rows, cols)
+    out = tb.matvec_axis0(to_dev_u32(codes), to_dev_f16(scales), to_dev_bf16(x), g, tb.new_workspace(M, g, "cuda"))
+    ref, ab = oracle_mod.matvec_axis0(codes, scales, x, k, 12, T)
+    check_band(oracle_mod, bf16_bits(out), ref, ab, f"axis0 L=12 k={k}")
+
+
+# Work ranges that cross column blocks (several segments per CTA), a single column block shared by many CTAs,
+# and staged pieces with a ragged last 8-row step.
+@pytest.mark.parametrize("k", [2, 3])
+@pytest.mark.parametrize("rows,cols,M", [(77, 256 * 40, 2), (5000, 256, 4), (1001, 1280, 1), (259, 512, 3)])
+def test_matvec_axis0_segments_and_pieces(oracle_mod, k, rows, cols, M):
+    codes, scales, x = inputs.make_linear(rows, cols, k, M, seed_codes=71 + k, seed_x=72 + M, sigma=0.5,
+                                          x_len=rows)
+    g = tb.Geometry(k, L, T, 0, rows, cols)
+    out = tb.matvec_axis0(to_dev_u32(codes), to_dev_f16(scales), to_dev_bf16(x), g, tb.new_workspace(M, g, "cuda"))
+    ref, ab = oracle_mod.matvec_axis0(codes, scales, x, k, L, T)
+    check_band(oracle_mod, bf16_bits(out), ref, ab, f"axis0 segments k={k} M={M} {rows}x{cols}")
+
+
+def test_matvec_axis0_long_ranges(oracle_mod):
+    """Each CTA's range is longer than one tensor-core accumulation chain (100000 rows over at most 256 CTAs)."""
+    rows, cols, M, k = 100000, 1024, 2, 2
+    codes, scales, x = inputs.make_linear(rows, cols, k, M, seed_codes=81, seed_x=82, sigma=0.5, x_len=rows)
+    g = tb.Geometry(k, L, T, 0, rows, cols)
+    out = bf16_bits(tb.matvec_axis0(to_dev_u32(codes), to_dev_f16(scales), to_dev_bf16(x), g,
+                                    tb.new_workspace(M, g, "cuda")))
+    idx = _sample(cols, 24, 83)
+    ref, ab = oracle_mod.matvec_axis0(codes, scales, x, k, L, T, cols=idx)
+    check_band(oracle_mod, out[:, idx], ref, ab, "axis0 long ranges")
 
 
 def test_matvec_axis0_is_deterministic():

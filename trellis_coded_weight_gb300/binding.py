@@ -30,7 +30,7 @@ EXPORTS = ("trellis_abi_version", "trellis_status_string", "trellis_check_geom",
            "trellis_matvec_axis1", "trellis_matvec_axis0", "trellis_workspace_bytes", "trellis_gateup_swiglu",
            "trellis_gemm_prefill", "trellis_device_error", "trellis_mlp_decode", "trellis_matvec_axis1_bf16w",
            "trellis_matvec_axis0_bf16w", "trellis_load_floor", "trellis_load_floor_rows", "trellis_prefill_plan",
-           "trellis_set_wait_limit")
+           "trellis_set_wait_limit", "trellis_matvec_axis1_host")
 
 
 class TrellisGeom(ctypes.Structure):
@@ -111,6 +111,8 @@ def load(path: str = LIB_PATH):
             lib.trellis_gateup_swiglu.argtypes = [vp, vp, vp, vp, vp, vp, i32, g, vp]
             lib.trellis_gemm_prefill.restype = i32
             lib.trellis_gemm_prefill.argtypes = [vp, vp, vp, vp, i32, g, vp]
+            lib.trellis_matvec_axis1_host.restype = i32
+            lib.trellis_matvec_axis1_host.argtypes = [vp, vp, vp, vp, i32, g, vp, vp, vp]
             lib.trellis_matvec_axis1_bf16w.restype = i32
             lib.trellis_matvec_axis1_bf16w.argtypes = [vp, vp, vp, vp, i32, g, vp]
             lib.trellis_matvec_axis0_bf16w.restype = i32
@@ -190,6 +192,35 @@ def matvec_axis1(codes, scales, x, g: Geometry, out=None, bf16_weights: bool = F
     with _on(x):
         _check(fn, getattr(load(), fn)(*args, M, ctypes.byref(g.c()), _stream(x)))
     return out
+
+
+def _req_host(t: torch.Tensor, name: str, shape):
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if t.dtype != torch.bfloat16:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected torch.bfloat16")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def matvec_axis1_host(codes, scales, x_host, g: Geometry, out_host, x_dev, out_dev):
+    """matvec_axis1 with x and out on the host: one C call queues x_host -> x_dev, the matvec into out_dev and
+    out_dev -> out_host on the current stream of the codes' device.  out_host holds the result once that stream
+    has reached the call (synchronize before reading it).  Pinned host tensors keep the copies asynchronous."""
+    M = x_host.shape[0]
+    args = (_req(codes, "codes", _CODES, g.codes_shape),
+            _req(scales, "scales", (torch.float16,), (g.rows,)),
+            _req_host(x_host, "x_host", (M, g.cols)),
+            _req_host(out_host, "out_host", (M, g.rows)))
+    xd = _req(x_dev, "x_dev", (torch.bfloat16,), (M, g.cols))
+    od = _req(out_dev, "out_dev", (torch.bfloat16,), (M, g.rows))
+    with _on(codes):
+        _check("trellis_matvec_axis1_host",
+               load().trellis_matvec_axis1_host(*args, M, ctypes.byref(g.c()), xd, od, _stream(codes)))
+    return out_host
 
 
 def workspace_bytes(M: int, g: Geometry) -> int:

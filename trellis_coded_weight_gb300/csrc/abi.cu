@@ -106,6 +106,24 @@ int trellis_matvec_axis1(const uint32_t* codes, const uint16_t* scales, const ui
                                                   static_cast<cudaStream_t>(stream)));
 }
 
+int trellis_matvec_axis1_host(const uint32_t* codes, const uint16_t* scales, const uint16_t* x_host,
+                              uint16_t* out_host, int M, const trellis_geom_t* g, uint16_t* x_dev, uint16_t* out_dev,
+                              trellis_stream_t stream) {
+  int st = geom_ok(g);
+  if (st) return st;
+  if (g->axis != 1) return TRELLIS_EAXIS;
+  if (M < 1 || M > 4) return TRELLIS_EM;
+  if (!codes || !scales || !x_host || !out_host || !x_dev || !out_dev) return TRELLIS_ENULL;
+  if (!aligned16(codes) || !aligned16(scales) || !aligned16(x_dev) || !aligned16(out_dev)) return TRELLIS_EALIGN;
+  if ((st = device_ok())) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t xb = (size_t)M * (size_t)g->cols * sizeof(uint16_t), ob = (size_t)M * (size_t)g->rows * sizeof(uint16_t);
+  if (cudaMemcpyAsync(x_dev, x_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess) return TRELLIS_ECUDA;
+  if (trellis::launch_matvec_axis1(codes, scales, x_dev, out_dev, M, g->k, g->L, g->rows, g->cols, s) != cudaSuccess)
+    return TRELLIS_ECUDA;
+  return cuda_status(cudaMemcpyAsync(out_host, out_dev, ob, cudaMemcpyDeviceToHost, s));
+}
+
 int trellis_matvec_axis1_bf16w(const uint32_t* codes, const uint16_t* scales, const uint16_t* x, uint16_t* out,
                                int M, const trellis_geom_t* g, trellis_stream_t stream) {
   int st = geom_ok(g);

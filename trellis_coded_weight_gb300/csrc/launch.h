@@ -48,11 +48,20 @@ cudaError_t launch_gateup_swiglu(const uint32_t* gcodes, const uint16_t* gscales
                                  int L, int64_t rows, int64_t cols, cudaStream_t st);
 
 // Workspace of the axis-0 matvec: fp32 partials followed by per-column-block
-// arrival counters.
+// arrival counters.  launch_matvec_axis0 takes the tensor-core kernel for M >= 3
+// and the CUDA-core kernel for M <= 2.
 size_t axis0_workspace_bytes(int M, int64_t rows, int64_t cols);
 cudaError_t launch_matvec_axis0(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
                                 uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols, int interleave,
                                 void* workspace, cudaStream_t st);
+// The two kernels behind it (same workspace layout): y * x*scale on the tensor cores (matvec_axis0_tc.cu, every
+// M), or packed fp32 FMA on the CUDA cores (matvec_axis0.cu, every M; also the bf16-weight variant's kernel).
+cudaError_t launch_matvec_axis0_tc(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
+                                   uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols, int interleave,
+                                   void* workspace, cudaStream_t st);
+cudaError_t launch_matvec_axis0_fma(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
+                                    uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols, int interleave,
+                                    void* workspace, cudaStream_t st);
 
 cudaError_t launch_gemm_prefill(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
                                 uint16_t* out, int M, int k, int L, int axis, int64_t rows, int64_t cols,

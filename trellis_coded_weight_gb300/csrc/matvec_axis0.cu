@@ -23,15 +23,12 @@
 //     pieces of at most kAx0StageRows rows) and read with a broadcast load per
 //     row; 1/d is applied after the sum.
 //   * at the end of a segment the CTA folds its warps in shared memory and
-//     writes one fp32 partial per output to the workspace, in slot c + cb
-//     (unique per CTA and column block).  Arrivals are published at the end
-//     of the range (one fence for all its segments).  The last CTA to arrive
-//     for a column block (an atomic counter against the known number of CTAs
-//     that cover it) folds the partials in CTA order, stores bf16 and resets
-//     the counter -- one launch, deterministic, no atomics on data.
+//     writes one fp32 partial per output to the workspace; the partials are
+//     folded deterministically in one launch (axis0_split.cuh).
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "axis0_split.cuh"
 #include "common.cuh"
 #include "devcache.h"
 #include "launch.h"
@@ -39,10 +36,7 @@
 namespace trellis {
 
 constexpr int kAx0Chunk = 4;             // rows per lane per prefetch group
-constexpr int kAx0MaxCtas = 256;         // bound on the grid (sizes the workspace)
-constexpr int64_t kAx0MinRows = 64;      // fewest (column block, row) pairs per CTA
 constexpr int64_t kAx0StageRows = 2048;  // rows of x*scale staged at once
-constexpr int kAx0MaxPending = 4;        // segments whose arrival waits for one fence
 
 // Warps per CTA: as many as the accumulators' registers allow with one CTA per SM.
 template <int M>
@@ -54,21 +48,6 @@ size_t axis0_workspace_bytes(int M, int64_t rows, int64_t cols) {
   const size_t part = (size_t)(kAx0MaxCtas + nb) * (size_t)M * kT * sizeof(float);
   return part + (((size_t)nb * sizeof(uint32_t) + 15) & ~(size_t)15);
 }
-
-struct Ax0Params {
-  const uint32_t* codes;
-  const uint16_t* scales;
-  const uint16_t* x;
-  uint16_t* out;
-  float* part;        // [kAx0MaxCtas + nb][M][256]
-  uint32_t* counter;  // [nb]
-  int64_t R, C, N;    // rows, cols, N = nb * R work items
-  int nb, G;          // column blocks, CTAs
-  int stage;          // rows staged at once (<= kAx0StageRows)
-};
-
-// The CTA whose range holds work item f: the largest c with c*N/G <= f.
-__device__ __forceinline__ int ax0_cta_of(int64_t f, int64_t N, int G) { return (int)(((f + 1) * G - 1) / N); }
 
 template <int K, int L, int M, bool BW, bool IL>
 __global__ void __launch_bounds__(32 * ax0_warps<M>(), 1) ax0_kernel(const Ax0Params p) {
@@ -264,48 +243,7 @@ __global__ void __launch_bounds__(32 * ax0_warps<M>(), 1) ax0_kernel(const Ax0Pa
       for (int w = 1; w < W; ++w) v += red[w * M * kT + i];
       slot[i] = v;
     }
-    // Arrival is deferred: a range that crosses column blocks publishes all
-    // its partials with one fence at the end instead of one per segment.
-    if (threadIdx.x == 0) pend[npend] = cb;
-    if (++npend == kAx0MaxPending || f >= f1) {
-      __threadfence();
-      __syncthreads();
-      if (threadIdx.x == 0)
-        for (int i = 0; i < npend; ++i) {
-          const int pc = pend[i];
-          const int first = ax0_cta_of((int64_t)pc * p.R, p.N, p.G);
-          const int last = ax0_cta_of((int64_t)pc * p.R + p.R - 1, p.N, p.G);
-          is_last[i] = (atomicAdd(p.counter + pc, 1u) == (uint32_t)(last - first)) ? 1u : 0u;
-        }
-      __syncthreads();
-      for (int i = 0; i < npend; ++i) {
-        if (!is_last[i]) continue;
-        // the last CTA to arrive folds the column block's partials in CTA order
-        __threadfence();
-        const int pc = pend[i];
-        const int first = ax0_cta_of((int64_t)pc * p.R, p.N, p.G);
-        const int ns = ax0_cta_of((int64_t)pc * p.R + p.R - 1, p.N, p.G) - first + 1;
-        const float* ps = p.part + (int64_t)(first + pc) * M * kT;
-        for (int e = threadIdx.x; e < M * kT; e += blockDim.x) {
-          float v = 0.f;
-          for (int s0 = 0; s0 < ns; s0 += 16) {
-            float q[16];
-#pragma unroll
-            for (int u = 0; u < 16; ++u) q[u] = (s0 + u < ns) ? __ldcg(ps + (int64_t)(s0 + u) * M * kT + e) : 0.f;
-#pragma unroll
-            for (int u = 0; u < 16; ++u)
-              if (s0 + u < ns) v += q[u];
-          }
-          const int m = e / kT, t = e - m * kT;
-          uint16_t o;
-          asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(o) : "f"(BW ? v : __fmul_rn(v, kRcpD)));
-          p.out[(int64_t)m * p.C + (int64_t)pc * kT + t] = o;
-        }
-        if (threadIdx.x == 0) p.counter[pc] = 0u;
-      }
-      npend = 0;
-    }
-    __syncthreads();  // red, pend and is_last are reused by the next segment
+    ax0_publish<M, BW>(p, pend, is_last, npend, cb, f >= f1);
   }
 }
 
@@ -355,12 +293,8 @@ static cudaError_t ax0_dispatch(const uint32_t* codes, const uint16_t* scales, c
   p.counter = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) +
                                           (size_t)(kAx0MaxCtas + p.nb) * (size_t)M * kT * sizeof(float));
   p.R = rows; p.C = cols; p.N = (int64_t)p.nb * rows;
-  int64_t G = device_sm_count();
-  if (G > kAx0MaxCtas) G = kAx0MaxCtas;
-  if (G > (p.N + kAx0MinRows - 1) / kAx0MinRows) G = (p.N + kAx0MinRows - 1) / kAx0MinRows;
-  if (G < 1) G = 1;
-  p.G = (int)G;
-  const int64_t per = (p.N + G - 1) / G;  // longest range, hence longest segment
+  p.G = ax0_grid(p.N);
+  const int64_t per = (p.N + p.G - 1) / p.G;  // longest range, hence longest segment
   p.stage = (int)(per < kAx0StageRows ? per : kAx0StageRows);
   const bool il = interleave != 0;
   if (L == 16) {
@@ -373,9 +307,9 @@ static cudaError_t ax0_dispatch(const uint32_t* codes, const uint16_t* scales, c
   return ax0_launch_m<4, 12, BW>(p, M, il, st);
 }
 
-cudaError_t launch_matvec_axis0(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
-                                uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols, int interleave,
-                                void* workspace, cudaStream_t st) {
+cudaError_t launch_matvec_axis0_fma(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
+                                    uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols, int interleave,
+                                    void* workspace, cudaStream_t st) {
   return ax0_dispatch<false>(codes, scales, x, out, M, k, L, rows, cols, interleave, workspace, st);
 }
 
@@ -383,6 +317,16 @@ cudaError_t launch_matvec_axis0_bf16w(const uint32_t* codes, const uint16_t* sca
                                       uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols, int interleave,
                                       void* workspace, cudaStream_t st) {
   return ax0_dispatch<true>(codes, scales, x, out, M, k, L, rows, cols, interleave, workspace, st);
+}
+
+// M >= 3 on the tensor cores, M <= 2 on the CUDA cores: at 17408 x 5120 (k = 2 / 3 / 4) the tensor-core kernel
+// costs about the same for every M (34.7-36.8 / 38.9-40.8 / 34.9-37.5 us) while this kernel grows with M
+// (28.6, 32.8, 38.1, 40.6 us at k = 2), so they cross between M = 2 and M = 3.
+cudaError_t launch_matvec_axis0(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
+                                uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols, int interleave,
+                                void* workspace, cudaStream_t st) {
+  if (M >= 3) return launch_matvec_axis0_tc(codes, scales, x, out, M, k, L, rows, cols, interleave, workspace, st);
+  return launch_matvec_axis0_fma(codes, scales, x, out, M, k, L, rows, cols, interleave, workspace, st);
 }
 
 }  // namespace trellis

@@ -36,6 +36,7 @@
 #include "common.cuh"
 #include "devcache.h"
 #include "launch.h"
+#include "mma_tf32.cuh"
 
 namespace trellis {
 namespace {
@@ -44,22 +45,6 @@ constexpr int kRowGroups = 4;    // 16-row groups per CTA (64 rows)
 constexpr int kTStride = 264;    // bytes per lane-quarter (64 fp32 positions) of one token's block, padded
 constexpr int kTokStride = 1056; // bytes per token per block (4 quarters)
 constexpr int kZeroBytes = 512;  // zero area for absent tokens: lanes read 32*M + 8j, j < 32
-
-__device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// y of state s as fp32 bits (exact): through an int-to-float conversion (ALU pipe) or through the float bias
-// 1.5*2^23 and its subtraction (FMA pipe).  The kernel takes row g one way and row g+8 the other, which
-// balances the two pipes (the window extraction also runs on the ALU pipe).
-template <bool ALU>
-__device__ __forceinline__ uint32_t code_f32(uint32_t s) {
-  return __float_as_uint(ALU ? __int2float_rn(code_int(s)) : code_y(s));
-}
 
 // A lane's 2K words of one block (positions [64t, 64t+64)) with 16-byte loads.  For K = 3 the 24 bytes start on
 // an 8-byte boundary: two aligned 16-byte loads cover them and the lane keeps the right 6 words.
