@@ -657,13 +657,22 @@ def main():
 
     # roofline of the dominant kernel: the axis-1 matvec (every timed launch is one).  Bound by HBM in the
     # metric's terms: algorithmic bytes per launch over the mean launch time against the measured copy rate.
-    achieved = sum(alg.values()) / (sum(per.values()) * 1e-3) / 1e9
+    # The mean launch time is the timed region's events over its launches (back-to-back, as the step runs
+    # them); the second pass's event pair around every launch also gives it, but those events stop each
+    # launch from overlapping the previous one's end (programmatic dependent launch), so that figure is
+    # reported beside it.
+    step_s = res["ms_total"] * 1e-3 / args.steps  # one rank's step (each rank runs the same step)
+    achieved = sum(alg.values()) / step_s / 1e9
+    achieved_events = sum(alg.values()) / (sum(per.values()) * 1e-3) / 1e9
     prof = [measured_profile(f"axis1_k{k}_M{M}") for k in KS for M in MS]
     traffic = (sum(p["dram_bytes_per_launch"] for p in prof) / len(prof)) if all(prof) else None
     floors = {r["kind"] + f"_k{r['k']}": packed_bytes(r["k"]) / (r["us"] * 1e-6) / 1e9
               for r in res.get("rows", []) if r["kind"].startswith("load_floor")}
     roofline = {"kernel": "trellis_matvec_axis1 (mv1_kernel at M = 1, mvtc_kernel at M >= 2)", "bound": "hbm",
                 "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "mean_launch_us": step_s / len(alg) * 1e6,
+                "achieved_per_launch_events": {"value": achieved_events, "frac": achieved_events / hbm,
+                                               "mean_launch_us": sum(per.values()) / len(per) * 1e3},
                 "peak_source": f"{peak_src} hbm_gbs (copy)",
                 "algorithmic_bytes_per_launch": sum(alg.values()) / len(alg),
                 "traffic": traffic, "load_floor_GBps": floors}
@@ -674,7 +683,7 @@ def main():
         sms = torch.cuda.get_device_properties(0).multi_processor_count
         mhz = float(res["clocks_all"].get("sm_max_mhz") or 2070.0)
         inst = sum(p["warp_instructions_per_launch"] for p in prof)
-        ach = inst / (sum(per.values()) * 1e-3) / 1e12
+        ach = inst / step_s / 1e12
         peak_i = sms * 4 * mhz * 1e6 / 1e12
         roofline["issue"] = {"achieved": ach, "peak": peak_i, "unit": "T warp-instructions/s", "frac": ach / peak_i,
                              "peak_source": f"derived: {sms} SMs x 4 schedulers x 1 instruction/clock x {mhz:.0f} MHz",

@@ -32,6 +32,7 @@
 #include "common.cuh"
 #include "devcache.h"
 #include "launch.h"
+#include "pdl.cuh"
 
 namespace trellis {
 
@@ -60,6 +61,7 @@ __global__ void __launch_bounds__(32 * ax0_warps<M>(), 1) ax0_kernel(const Ax0Pa
   constexpr int G = kAx0Chunk;
   constexpr int RS = 2 * W;  // rows per CTA step
   extern __shared__ __align__(16) float smem[];
+  pdl_enter();
   float* xs = smem;                                       // [stage][M]  x*scale of the staged rows
   float* red = smem + ((p.stage * M + 3) & ~3);           // [W][M][256], 16-byte aligned
   float* scs = red + W * M * kT;                          // [stage] row scales (bf16-weight numerics)
@@ -261,8 +263,8 @@ static cudaError_t ax0_launch1(const Ax0Params& p, cudaStream_t st) {
     return cudaFuncSetAttribute(ax0_kernel<K, L, M, BW, IL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
   }, cudaErrorInvalidDevice);
   if (attr_err != cudaSuccess) return attr_err;
-  ax0_kernel<K, L, M, BW, IL><<<p.G, 32 * W, smem, st>>>(p);
-  return cudaGetLastError();
+  const cudaError_t e = launch_pdl(ax0_kernel<K, L, M, BW, IL>, dim3(p.G), dim3(32 * W), smem, st, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int K, int L, bool BW, bool IL>

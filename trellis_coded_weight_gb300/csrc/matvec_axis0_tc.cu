@@ -36,6 +36,7 @@
 #include "devcache.h"
 #include "launch.h"
 #include "mma_tf32.cuh"
+#include "pdl.cuh"
 
 namespace trellis {
 namespace {
@@ -171,6 +172,7 @@ __global__ void __launch_bounds__(32 * kA0tWarps, 1) ax0tc_kernel(const Ax0Param
   constexpr int kPieceSteps = P / 8 / kA0tSlices;  // k-steps of a warp in a full piece
   constexpr int kCopyRows = 32 * kA0tWarps / CH;  // rows one pass of the CTA's 16-byte copies covers
   extern __shared__ __align__(16) unsigned char smem[];
+  pdl_enter();
   uint32_t* cbuf = reinterpret_cast<uint32_t*>(smem);             // [kA0tBufs][P][ST] code words
   float* xsb = reinterpret_cast<float*>(cbuf + kA0tBufs * P * ST);  // [kA0tBufs][P/8][4][8][2] B operands
   float* red = xsb + kA0tBufs * P * 8;                             // [kA0tSlices][M][256]
@@ -379,8 +381,8 @@ cudaError_t a0t_launch1(const Ax0Params& p, cudaStream_t st) {
     return cudaFuncSetAttribute(ax0tc_kernel<K, L, M, IL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   }, cudaErrorInvalidDevice);
   if (attr_err != cudaSuccess) return attr_err;
-  ax0tc_kernel<K, L, M, IL><<<p.G, 32 * kA0tWarps, smem, st>>>(p);
-  return cudaGetLastError();
+  const cudaError_t e = launch_pdl(ax0tc_kernel<K, L, M, IL>, dim3(p.G), dim3(32 * kA0tWarps), smem, st, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int K, int L, bool IL>

@@ -31,6 +31,7 @@
 #include "common.cuh"
 #include "devcache.h"
 #include "launch.h"
+#include "pdl.cuh"
 
 namespace trellis {
 
@@ -72,6 +73,7 @@ __device__ __forceinline__ void load_half(HalfBlock<K, NMAT>& hbk, const uint32_
 template <int K, int L, int M, bool GU, bool BW>
 __global__ void __launch_bounds__(512) mv1_kernel(const Mv1Params p) {
   extern __shared__ __align__(16) float smem[];
+  pdl_enter();
   constexpr int NMAT = GU ? 2 : 1;
   constexpr int WPB = kT * K / 32;
   constexpr int HB = kT / 2;  // positions per half block
@@ -217,8 +219,8 @@ static cudaError_t mv1_launch(const Mv1Params& p, cudaStream_t st) {
   const int nmat = GU ? 2 : 1;
   const size_t sm = (size_t)S * M * (kT / 2) * sizeof(float) + (size_t)nmat * S * M * 32 * sizeof(float);
   const dim3 grid((unsigned)((p.R + 31) / 32)), block(32 * S);
-  mv1_kernel<K, L, M, GU, BW><<<grid, block, sm, st>>>(p);
-  return cudaGetLastError();
+  const cudaError_t e = launch_pdl(mv1_kernel<K, L, M, GU, BW>, grid, block, sm, st, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int K, int L, bool GU, bool BW>

@@ -37,6 +37,7 @@
 #include "devcache.h"
 #include "launch.h"
 #include "mma_tf32.cuh"
+#include "pdl.cuh"
 
 namespace trellis {
 namespace {
@@ -93,6 +94,7 @@ __global__ void __launch_bounds__(TcCfg<K, L, M, GU>::Threads, 2)
   constexpr int WPB = 8 * K;
   constexpr int NW = 2 * K + 1;
   extern __shared__ __align__(128) unsigned char smem[];
+  pdl_enter();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
   const int rg = warp % kRowGroups, ks = (warp / kRowGroups) % KS, mt = warp / (kRowGroups * KS);
@@ -227,8 +229,9 @@ cudaError_t tc_launch(const uint32_t* c0, const uint16_t* s0, const uint32_t* c1
   const int nb = (int)(C / kT);
   const int SB = nb < Cfg::SBMax ? nb : Cfg::SBMax;
   const unsigned grid = (unsigned)((R + 16 * kRowGroups - 1) / (16 * kRowGroups));
-  kern<<<grid, Cfg::Threads, Cfg::smem(SB), st>>>(c0, s0, c1, s1, x, out, R, C, SB);
-  return cudaGetLastError();
+  const cudaError_t e = launch_pdl(kern, dim3(grid), dim3(Cfg::Threads), Cfg::smem(SB), st, c0, s0, c1, s1, x, out,
+                                   R, C, SB);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int K, int L, bool GU>
