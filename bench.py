@@ -296,52 +296,72 @@ def run_gpu(args):
 def run_e2e(args, torch, tdist, tb, dev, stream, bufs, scales, geoms, xs, rot, world, sync_all):
     """The headline through the C ABI with host buffers: each launch is one trellis_matvec_axis1_host call, which
     queues the copy of its x from pinned host memory, the matvec and the copy of its output back to pinned host
-    memory, in order on the launching stream.  Each (k, M) slot has its own host and device buffers; the
-    arguments are prepared once (pointers, geometry, stream), as for the device-timed headline."""
+    memory, in order on its stream.  Each (k, M) slot has its own host and device buffers; the arguments are
+    prepared once (pointers, geometry, stream), as for the device-timed headline.
+
+    `value` runs every call on the launching stream, so the matvecs run one after another as in the
+    device-timed step, each behind its copies.  `two_streams` alternates the slots between two streams: one
+    slot's copies then overlap the other stream's matvec, and matvecs of the two streams may also overlap one
+    another, which the one-stream figure excludes."""
     lib = tb.load()
     slots = [(k, M) for k in KS for M in MS]
     x_host = {M: xs[M].cpu().pin_memory() for M in MS}
     o_host = {s: torch.empty((s[1], R), dtype=torch.bfloat16).pin_memory() for s in slots}
     x_dev = {s: torch.empty_like(xs[s[1]]) for s in slots}
     o_dev = {s: torch.empty((s[1], R), dtype=torch.bfloat16, device=dev) for s in slots}
-    sptr = stream.cuda_stream
-    cargs = {}
-    for (k, M) in slots:  # the binding's checks once, then the prepared C arguments per code buffer
-        tb.matvec_axis1_host(bufs[k][0], scales[k], x_host[M], geoms[k], o_host[(k, M)], x_dev[(k, M)],
-                             o_dev[(k, M)])
-        for i, b in enumerate(bufs[k]):
-            cargs[(k, M, i)] = (b.data_ptr(), scales[k].data_ptr(), x_host[M].data_ptr(), o_host[(k, M)].data_ptr(),
-                                M, ctypes.byref(geoms[k].c()), x_dev[(k, M)].data_ptr(), o_dev[(k, M)].data_ptr(),
-                                sptr)
     fn = lib.trellis_matvec_axis1_host
 
-    def e2e_step():
-        for (k, M) in slots:
-            i = rot[k]
-            rot[k] = (i + 1) % len(bufs[k])
-            st = fn(*cargs[(k, M, i)])
-            if st:
-                raise RuntimeError(f"trellis_matvec_axis1_host returned {st}")
+    def timed(streams):
+        cargs = {}
+        for j, (k, M) in enumerate(slots):  # the binding's checks once, then the prepared C arguments
+            sp = streams[j % len(streams)]
+            with torch.cuda.stream(sp):
+                tb.matvec_axis1_host(bufs[k][0], scales[k], x_host[M], geoms[k], o_host[(k, M)], x_dev[(k, M)],
+                                     o_dev[(k, M)])
+            for i, b in enumerate(bufs[k]):
+                cargs[(k, M, i)] = (b.data_ptr(), scales[k].data_ptr(), x_host[M].data_ptr(),
+                                    o_host[(k, M)].data_ptr(), M, ctypes.byref(geoms[k].c()), x_dev[(k, M)].data_ptr(),
+                                    o_dev[(k, M)].data_ptr(), sp.cuda_stream)
 
-    for _ in range(args.warmup):
-        e2e_step()
-    sync_all()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    b.record(stream)  # after the last output's copy to the host
-    sync_all()
-    e2e_ms = a.elapsed_time(b)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    step_bytes = sum(packed_bytes(k) for k in KS for M in MS)
-    return {"value": world * step_bytes * args.steps / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+        def e2e_step():
+            for (k, M) in slots:
+                i = rot[k]
+                rot[k] = (i + 1) % len(bufs[k])
+                st = fn(*cargs[(k, M, i)])
+                if st:
+                    raise RuntimeError(f"trellis_matvec_axis1_host returned {st}")
+
+        for _ in range(args.warmup):
+            e2e_step()
+        sync_all()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for sp in streams:
+            if sp is not stream:
+                sp.wait_event(a)
+        for _ in range(args.steps):
+            e2e_step()
+        for sp in streams:
+            if sp is not stream:
+                stream.wait_stream(sp)
+        b.record(stream)  # after the last output's copy to the host
+        sync_all()
+        ms = a.elapsed_time(b)
+        if world > 1:
+            tt = torch.tensor([ms], device=dev, dtype=torch.float64)
+            tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
+            ms = float(tt.item())
+        return world * sum(packed_bytes(k) for k in KS for M in MS) * args.steps / (ms * 1e-3) / 1e9
+
+    one = timed([stream])
+    two = timed([torch.cuda.Stream(dev), torch.cuda.Stream(dev)])
+    return {"value": one, "unit": "GB/s",
             "h2d_bytes_per_step": sum(M * C * 2 for k in KS for M in MS),
             "d2h_bytes_per_step": sum(M * R * 2 for k in KS for M in MS),
-            "call": "trellis_matvec_axis1_host (one C call per launch: x in, matvec, out back, on one stream)"}
+            "call": "trellis_matvec_axis1_host (one C call per launch: x in, matvec, out back), all on one stream",
+            "two_streams": {"value": two, "unit": "GB/s",
+                            "how": "the same calls alternating between two streams: copies overlap the other "
+                                   "stream's matvec, and the two streams' matvecs may overlap"}}
 
 
 def run_rows(torch, tb, inputs, dev, timer, l2, bufs, scales, geoms):
