@@ -310,3 +310,36 @@ def test_load_floors_fold_the_words_they_read(k):
     keep[0] = keep[4 * k] = False
     want = np.bitwise_xor.reduce(codes.reshape(rows, -1, wpb)[:, :, keep].reshape(rows, -1), axis=1)
     assert np.array_equal(tb.load_floor(dc, g).cpu().numpy().view(np.uint32), want)
+
+
+# ------------------------------------------------------------------ back-to-back launches
+
+@pytest.mark.parametrize("consumer_axis", [1, 0])
+def test_chained_matvecs_read_the_previous_output(oracle_mod, consumer_axis):
+    """A matvec whose x is the output of the matvec just ahead of it on the stream (both launched with
+    programmatic dependent launch): the consumer must see the producer's finished output.  Repeated with
+    fresh inputs so that a consumer reading early would see stale values."""
+    M, k = 4, 2
+    r1, c1 = 1024, 768  # producer: out1 [M, 1024]
+    codes1, scales1, _ = inputs.make_linear(r1, c1, k, M, seed_codes=101, seed_x=102)
+    if consumer_axis == 1:
+        r2, c2 = 512, r1  # consumer reads out1 as x [M, 1024]
+        codes2, scales2, _ = inputs.make_linear(r2, c2, k, M, seed_codes=103, seed_x=104)
+        g2 = tb.Geometry(k, L, T, 1, r2, c2)
+    else:
+        r2, c2 = r1, 512  # axis-0 consumer: stored rows = 1024 = len(x)
+        codes2, scales2, _ = inputs.make_linear(r2, c2, k, M, seed_codes=105, seed_x=106, x_len=r2)
+        g2 = tb.Geometry(k, L, T, 0, r2, c2)
+    g1 = tb.Geometry(k, L, T, 1, r1, c1)
+    d1c, d1s, d2c, d2s = to_dev_u32(codes1), to_dev_f16(scales1), to_dev_u32(codes2), to_dev_f16(scales2)
+    ws = tb.new_workspace(M, g2, "cuda") if consumer_axis == 0 else None
+    for rep in range(3):
+        x = inputs.normal_bf16(110 + rep, (M, c1))
+        out1 = tb.matvec_axis1(d1c, d1s, to_dev_bf16(x), g1)
+        out2 = tb.matvec_axis1(d2c, d2s, out1, g2) if consumer_axis == 1 else tb.matvec_axis0(d2c, d2s, out1, g2, ws)
+        mid = bf16_bits(out1)
+        if consumer_axis == 1:
+            ref, ab = oracle_mod.matvec_axis1(codes2, scales2, mid, k, L, T)
+        else:
+            ref, ab = oracle_mod.matvec_axis0(codes2, scales2, mid, k, L, T)
+        check_band(oracle_mod, bf16_bits(out2), ref, ab, f"chained axis1 -> axis{consumer_axis} rep {rep}")
