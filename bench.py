@@ -48,7 +48,7 @@ sys.path.insert(0, ROOT)
 METRIC = "packed-weight HBM GB/s (frac of GB300 peak) at M=1..4; prefill TFLOP/s at M=2048"
 R, C, L, T = 17408, 5120, 16, 256
 KS, MS = (2, 3, 4), (1, 2, 3, 4)
-PREFILL_M = (32, 512, 2048)
+PREFILL_M = (8, 16, 32, 512, 2048)  # 8 and 16: the register-decode path; 32 and up: tcgen05
 PREFILL0_M = (8, 64, 512, 2048)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -423,7 +423,8 @@ def run_rows(torch, tb, inputs, dev, timer, l2, bufs, scales, geoms):
         o = torch.empty((M, R), dtype=torch.bfloat16, device=dev)
         t = timer(lambda i: tb.gemm_prefill(cs[i], sc, x, g, o), len(cs))
         tc = timer(lambda i: torch.matmul(x, tb.expand_bf16(cs[i], sc, g, wtmp).t()), len(cs))
-        rows.append({"kind": "prefill", "config": 5, "k": k, "M": M, **t, "flops": 2.0 * M * R * C,
+        rows.append({"kind": "prefill", "config": 5 if M >= 32 else None, "k": k, "M": M, **t,
+                     "flops": 2.0 * M * R * C,
                      "comparator": {"what": "trellis_expand_bf16 + torch.matmul (cuBLAS)", **tc}})
     del cs
     # ---- axis-0 prefill (the down projection for M > 4), k = 3, stored W^T [17408 in, 5120 out] ----

@@ -259,7 +259,10 @@ int trellis_mlp_decode(const uint32_t *gcodes, const uint16_t *gscales, const ui
  * rows and stored transposed into the tile, and the long reduction over rows
  * is split across thread-block clusters where tiles alone would leave SMs
  * idle (possibly as a second launch on `stream` for the tiles left after
- * whole waves).  Results are deterministic: repeated calls give equal bits.
+ * whole waves).  Axis 1 with M <= 16 keeps the decoded weights in registers
+ * instead and multiplies with warp-level MMAs (mma.sync bf16, one or two
+ * 8-token tiles): the same numerics, no shared-memory weight tiles.  Results
+ * are deterministic: repeated calls give equal bits.
  * Requires M >= 1, no interleaved layout, and for axis 0 rows % 8 == 0.
  */
 int trellis_gemm_prefill(const uint32_t *codes, const uint16_t *scales, const uint16_t *x,
@@ -303,9 +306,12 @@ int trellis_load_floor_rows(const uint32_t *codes, uint32_t *out, const trellis_
  * output features x tokens_per_tile tokens; tile t is feature tile
  * t % ceil(features/128), token tile t / ceil(features/128).
  *   launches: caller-owned, room for 2 launches (6 ints).
- * Returns the number of launches (1 or 2), or a negative status: the
- * geometry and M checks of trellis_gemm_prefill, ENULL, or EDEVICE when
- * sms < 1 and no usable device is current.
+ * Returns the number of launches (1 or 2); 0, with *tokens_per_tile = 0,
+ * when the call has no tiles: on axis 1 with M <= 16 trellis_gemm_prefill
+ * decodes into registers and multiplies with warp-level MMAs instead (64
+ * rows per thread block).  Or a negative status: the geometry and M checks
+ * of trellis_gemm_prefill, ENULL, or EDEVICE when sms < 1 and no usable
+ * device is current.
  */
 int trellis_prefill_plan(int M, const trellis_geom_t *g, int sms, int *tokens_per_tile, int *launches);
 

@@ -23,7 +23,8 @@ def _lib():
 
 
 @pytest.mark.parametrize("k", [2, 3, 4])
-@pytest.mark.parametrize("M,rows,cols", [(5, 128, 256), (32, 200, 768), (33, 128, 512), (100, 257, 1024),
+@pytest.mark.parametrize("M,rows,cols", [(5, 128, 256), (12, 77, 512), (16, 200, 5120), (17, 130, 768),
+                                         (32, 200, 768), (33, 128, 512), (100, 257, 1024),
                                          (300, 136, 512), (64, 64, 2048), (600, 130, 1024)])
 def test_prefill_small(oracle_mod, k, M, rows, cols):
     codes, scales, x = inputs.make_linear(rows, cols, k, M, seed_codes=61 + k, seed_x=62 + M)
@@ -63,6 +64,27 @@ def test_prefill_L12(oracle_mod):
     out = tb.gemm_prefill(to_dev_u32(codes), to_dev_f16(scales), to_dev_bf16(x), g)
     ref, ab = oracle_mod.prefill(codes, scales, x, 4, 12, T)
     check_band(oracle_mod, bf16_bits(out), ref, ab, "prefill L=12")
+
+
+@pytest.mark.parametrize("k", [2, 3, 4])
+def test_prefill_small_M_L12(oracle_mod, k):
+    """The register-decode path (axis 1, M <= 16) with 12-bit windows: neighbouring positions pair up."""
+    codes, scales, x = inputs.make_linear(70, 768, k, 9, seed_codes=5 + k)
+    g = tb.Geometry(k, 12, T, 1, 70, 768)
+    out = tb.gemm_prefill(to_dev_u32(codes), to_dev_f16(scales), to_dev_bf16(x), g)
+    ref, ab = oracle_mod.prefill(codes, scales, x, k, 12, T)
+    check_band(oracle_mod, bf16_bits(out), ref, ab, f"prefill L=12 k={k} M=9")
+
+
+@pytest.mark.parametrize("M", [8, 16])
+def test_prefill_small_M_full_size_sampled(oracle_mod, M):
+    rows, cols = 17408, 5120
+    codes, scales, x = inputs.make_linear(rows, cols, 2, M)
+    g = tb.Geometry(2, L, T, 1, rows, cols)
+    out = bf16_bits(tb.gemm_prefill(to_dev_u32(codes), to_dev_f16(scales), to_dev_bf16(x), g))
+    idx = np.sort(np.random.default_rng(M).choice(rows, 40, replace=False))
+    ref, ab = oracle_mod.prefill(codes, scales, x, 2, L, T, rows=idx)
+    check_band(oracle_mod, out[:, idx], ref, ab, f"prefill full M={M}")
 
 
 @pytest.mark.parametrize("k", [2, 3, 4])

@@ -39,14 +39,22 @@ def _stages(M, g):
     return -(-kd // bk)
 
 
-@pytest.mark.parametrize("M,tokens", [(1, 32), (5, 32), (32, 32), (33, 64), (64, 64), (65, 128), (128, 128),
+@pytest.mark.parametrize("M,tokens", [(17, 32), (32, 32), (33, 64), (64, 64), (65, 128), (128, 128),
                                       (129, 256), (256, 256), (257, 512), (2048, 512), (100000, 512)])
 def test_tokens_per_tile(M, tokens):
     bn, _ = tb.prefill_plan(M, tb.Geometry(2, 16, 256, 1, 17408, 5120), 152)
     assert bn == tokens
+    assert tb.prefill_plan(M, tb.Geometry(2, 16, 256, 0, 17408, 5120), 152)[0] == tokens
 
 
-@pytest.mark.parametrize("M", [5, 32, 512, 2048, 5000])
+@pytest.mark.parametrize("M", [1, 5, 16])
+def test_axis1_small_M_has_no_tiles(M):
+    # axis 1 with M <= 16 runs the register-decode kernel: no tile plan; axis 0 keeps its tiles
+    assert tb.prefill_plan(M, tb.Geometry(2, 16, 256, 1, 17408, 5120), 152) == (0, [])
+    assert tb.prefill_plan(M, tb.Geometry(2, 16, 256, 0, 17408, 5120), 152)[0] == 32
+
+
+@pytest.mark.parametrize("M", [17, 32, 512, 2048, 5000])
 def test_axis1_is_one_persistent_launch(M):
     g = tb.Geometry(2, 16, 256, 1, 17408, 5120)
     _, plan = tb.prefill_plan(M, g, 152)
@@ -87,6 +95,9 @@ def test_plan_invariants(sms, axis):
         g = tb.Geometry(3, 16, 256, axis, rows, cols)
         for M in (1, 31, 64, 200, 300, 512, 777, 1024, 2048, 4096):
             bn, plan = tb.prefill_plan(M, g, sms)
+            if axis == 1 and M <= 16:  # the register-decode kernel: no tiles
+                assert (bn, plan) == (0, [])
+                continue
             _, ntiles = _tiles(M, g)
             nk = _stages(M, g)
             assert bn == _tiles(M, g)[0]

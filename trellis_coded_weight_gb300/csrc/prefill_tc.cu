@@ -839,6 +839,10 @@ cudaError_t prefill_axis(const PrefillParams& p, const uint16_t* x, int k, int L
 int device_sm_count() { return sm_count(); }
 
 int prefill_plan(int M, int axis, int64_t nOut, int64_t Kd, int sms, int* tokens_per_tile, PrefillLaunch* launches) {
+  if (axis == 1 && M <= kPrefillSmallMaxM) {  // no tiles: the register-decode kernel (prefill_small.cu)
+    *tokens_per_tile = 0;
+    return 0;
+  }
   const int BN = M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : M <= 256 ? 256 : 512;
   const int BK = BN == 512 ? 32 : 64;
   const int nk = (int)((Kd + BK - 1) / BK);
@@ -864,6 +868,7 @@ int prefill_plan(int M, int axis, int64_t nOut, int64_t Kd, int sms, int* tokens
 
 cudaError_t launch_gemm_prefill(const uint32_t* codes, const uint16_t* scales, const uint16_t* x, uint16_t* out,
                                 int M, int k, int L, int axis, int64_t rows, int64_t cols, cudaStream_t st) {
+  if (axis == 1 && M <= kPrefillSmallMaxM) return launch_prefill_small(codes, scales, x, out, M, k, L, rows, cols, st);
   PrefillParams p{};
   p.codes = codes; p.scales = scales; p.out = out;
   p.R = rows; p.C = cols; p.M = M; p.nb = (int)(cols / kT);
