@@ -11,10 +11,16 @@ The same run times every other row of the hot path at its full size, each in
 `breakdown` with its median and p10/p90 launch time, its algorithmic bytes or
 FLOPs and its fraction of the measured peak: the fused gate/up SwiGLU layer
 (two 17408 x 5120 matrices, k = 2, 3), the axis-0 down projection (stored
-W^T 17408 x 5120, k = 2, 3), the bf16 expansion (k = 2..4), the tensor-core
-prefill GEMM (k = 2, M = 32 / 512 / 2048, next to expand + cuBLAS), the axis-0
+W^T 17408 x 5120, k = 2, 3), the bf16 expansion (k = 2..4), the prefill GEMM
+(k = 2, M = 8 / 16 / 32 / 512 / 2048, next to expand + cuBLAS), the axis-0
 prefill (k = 3, M = 8 / 64 / 512 / 2048, next to expand + cuBLAS), the decode
 MLP block as a CUDA graph, and two load-only floors of the packed stream.
+
+`e2e` is the headline's twelve launches through trellis_matvec_axis1_host, one
+C call per launch that copies its x in from pinned host memory and its output
+back, on one stream; `e2e.two_streams` the same calls alternating between two
+streams.  `roofline` is the axis-1 matvec's: algorithmic bytes per launch over
+the timed region's mean launch time, against the measured HBM copy rate.
 
 Inputs are seeded and synthetic (uniform random code words, fp16 scales
 U[0.005, 0.02], bf16 x ~ N(0,1), or N(0, 0.5) for the axis-0 input).  Code
