@@ -23,7 +23,7 @@ def _lib():
 
 
 @pytest.mark.parametrize("k", [2, 3, 4])
-@pytest.mark.parametrize("M,rows,cols", [(5, 128, 256), (12, 77, 512), (16, 200, 5120), (17, 130, 768),
+@pytest.mark.parametrize("M,rows,cols", [(1, 64, 512), (5, 128, 256), (12, 77, 512), (16, 200, 5120), (17, 130, 768),
                                          (32, 200, 768), (33, 128, 512), (100, 257, 1024),
                                          (300, 136, 512), (64, 64, 2048), (600, 130, 1024)])
 def test_prefill_small(oracle_mod, k, M, rows, cols):
@@ -88,7 +88,8 @@ def test_prefill_small_M_full_size_sampled(oracle_mod, M):
 
 
 @pytest.mark.parametrize("k", [2, 3, 4])
-@pytest.mark.parametrize("M,rows,cols", [(5, 256, 256), (40, 1000, 512), (300, 520, 768), (33, 8, 256)])
+@pytest.mark.parametrize("M,rows,cols", [(1, 64, 256), (5, 256, 256), (8, 1000, 512), (12, 8, 256), (16, 520, 768),
+                                         (40, 1000, 512), (300, 520, 768), (33, 8, 256)])
 def test_prefill_axis0_small(oracle_mod, k, M, rows, cols):
     """Axis 0 (stored W^T): out[m][c] = sum_r e(r,c) x[m][r] over bf16 expand weights."""
     codes, scales, x = inputs.make_linear(rows, cols, k, M, seed_codes=121 + k, seed_x=122, sigma=0.5, x_len=rows)
@@ -96,6 +97,31 @@ def test_prefill_axis0_small(oracle_mod, k, M, rows, cols):
     out = tb.gemm_prefill(to_dev_u32(codes), to_dev_f16(scales), to_dev_bf16(x), g)
     ref, ab = oracle_mod.matvec_axis0_bf16w(codes, scales, x, k, L, T)
     check_band(oracle_mod, bf16_bits(out), ref, ab, f"prefill axis0 k={k} M={M} {rows}x{cols}")
+
+
+@pytest.mark.parametrize("k", [2, 3, 4])
+def test_prefill_axis0_small_M_L12(oracle_mod, k):
+    """The register-decode path of axis 0 (M <= 16) with 12-bit windows."""
+    codes, scales, x = inputs.make_linear(296, 512, k, 11, seed_codes=9 + k, seed_x=10, sigma=0.5, x_len=296)
+    g = tb.Geometry(k, 12, T, 0, 296, 512)
+    out = tb.gemm_prefill(to_dev_u32(codes), to_dev_f16(scales), to_dev_bf16(x), g)
+    ref, ab = oracle_mod.matvec_axis0_bf16w(codes, scales, x, k, 12, T)
+    check_band(oracle_mod, bf16_bits(out), ref, ab, f"prefill axis0 L=12 k={k} M=11")
+
+
+@pytest.mark.parametrize("M", [8, 16])
+def test_prefill_axis0_small_M_full_size_sampled(oracle_mod, M):
+    """The down projection (17408 stored rows, 5120 outputs) at small M: 20 column blocks, each a cluster whose
+    CTAs split the 17408 rows and fold their partials; sampled outputs against the oracle, repeated calls equal."""
+    rows, cols, k = 17408, 5120, 3
+    codes, scales, x = inputs.make_linear(rows, cols, k, M, sigma=0.5, x_len=rows)
+    g = tb.Geometry(k, L, T, 0, rows, cols)
+    dc, ds, dx = to_dev_u32(codes), to_dev_f16(scales), to_dev_bf16(x)
+    first = tb.gemm_prefill(dc, ds, dx, g)
+    assert torch.equal(tb.gemm_prefill(dc, ds, dx, g).view(torch.int16), first.view(torch.int16))
+    idx = np.sort(np.random.default_rng(M + 1).choice(cols, 40, replace=False))
+    ref, ab = oracle_mod.matvec_axis0_bf16w(codes, scales, x, k, L, T, cols=idx)
+    check_band(oracle_mod, bf16_bits(first)[:, idx], ref, ab, f"prefill axis0 full M={M}")
 
 
 def test_prefill_axis0_split_is_deterministic():

@@ -66,17 +66,21 @@ cudaError_t launch_matvec_axis0_fma(const uint32_t* codes, const uint16_t* scale
 cudaError_t launch_gemm_prefill(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
                                 uint16_t* out, int M, int k, int L, int axis, int64_t rows, int64_t cols,
                                 cudaStream_t st);
-// The axis-1 prefill for M <= kPrefillSmallMaxM (prefill_small.cu): the decode in registers and mma.sync bf16;
-// launch_gemm_prefill takes it for those M.
+// The prefill for M <= kPrefillSmallMaxM: the decode in registers and mma.sync bf16, on axis 1
+// (prefill_small.cu) and on axis 0 (prefill_axis0_small.cu, clusters folding the split reduction); launch_gemm_prefill
+// takes them for those M.
 constexpr int kPrefillSmallMaxM = 16;
 cudaError_t launch_prefill_small(const uint32_t* codes, const uint16_t* scales, const uint16_t* x, uint16_t* out,
                                  int M, int k, int L, int64_t rows, int64_t cols, cudaStream_t st);
+cudaError_t launch_prefill_axis0_small(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
+                                       uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols,
+                                       cudaStream_t st);
 
 // Tile plan of the prefill GEMM (host arithmetic only): tokens per tile and up
 // to two launches over the output tiles, each [t0, t0 + count) with S CTAs per
 // tile (S > 1: a cluster splitting the tile's reduction).  Returns the number
-// of launches; 0 (and 0 tokens per tile) where the call takes the
-// register-decode kernel instead (axis 1, M <= kPrefillSmallMaxM).
+// of launches; 0 (and 0 tokens per tile) where the call takes a
+// register-decode kernel instead (M <= kPrefillSmallMaxM).
 struct PrefillLaunch {
   int t0, count, S;
 };
