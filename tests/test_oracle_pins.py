@@ -87,8 +87,8 @@ def _numpy_y(L):
 
 @pytest.mark.parametrize("L,lo,hi,distinct", [(16, -483, 469, 908), (12, -448, 454, 713)])
 def test_decode_regression_values(oracle_mod, L, lo, hi, distinct):
-    """Regression values of the code over all 2^L states, derived twice by
-    independent routes (enumeration here and a separate script): the range of y,
+    """Regression values of the code, fixed by enumerating all 2^L states
+    outside this repository's code: the range of y,
     the number of distinct y, and at L = 16 mean(y) = -0.0582 and
     var(y/d) = 1.00018 (the code is built to have unit variance; d is the
     fp32 rounding of sqrt(21845), the standard deviation of a sum of four
