@@ -15,16 +15,10 @@ cudaError_t launch_expand_bf16(const uint32_t* codes, const uint16_t* scales, ui
                                int64_t rows, int64_t cols, int interleave, cudaStream_t st);
 
 // Axis-1 matvec and fused gate/up (matvec_axis1_tc.cu): M = 1 on the CUDA cores, M >= 2 with y*x accumulated
-// on the tensor cores.  The _tc and _fma forms take one path for every M.
+// on the tensor cores.  The _fma forms take the CUDA-core path for every M.
 cudaError_t launch_matvec_axis1(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
                                 uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols,
                                 cudaStream_t st);
-cudaError_t launch_matvec_axis1_tc(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
-                                   uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols,
-                                   cudaStream_t st);
-cudaError_t launch_gateup_swiglu_tc(const uint32_t* gcodes, const uint16_t* gscales, const uint32_t* ucodes,
-                                    const uint16_t* uscales, const uint16_t* x, uint16_t* out, int M, int k,
-                                    int L, int64_t rows, int64_t cols, cudaStream_t st);
 // The same two layers with the accumulation on the CUDA cores (packed fp32 FMA, matvec_axis1.cu).
 cudaError_t launch_matvec_axis1_fma(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
                                     uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols,

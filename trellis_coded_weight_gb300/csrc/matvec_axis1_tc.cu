@@ -237,11 +237,11 @@ cudaError_t tc_launch(const uint32_t* c0, const uint16_t* s0, const uint32_t* c1
 template <int K, int L, bool GU>
 cudaError_t tc_launch_m(int M, const uint32_t* c0, const uint16_t* s0, const uint32_t* c1, const uint16_t* s1,
                         const uint16_t* x, uint16_t* out, int64_t R, int64_t C, cudaStream_t st) {
-  switch (M) {
-    case 1: return tc_launch<K, L, 1, GU>(c0, s0, c1, s1, x, out, R, C, st);
+  switch (M) {  // M = 1 takes the CUDA-core kernel
     case 2: return tc_launch<K, L, 2, GU>(c0, s0, c1, s1, x, out, R, C, st);
     case 3: return tc_launch<K, L, 3, GU>(c0, s0, c1, s1, x, out, R, C, st);
-    default: return tc_launch<K, L, 4, GU>(c0, s0, c1, s1, x, out, R, C, st);
+    case 4: return tc_launch<K, L, 4, GU>(c0, s0, c1, s1, x, out, R, C, st);
+    default: return cudaErrorInvalidValue;
   }
 }
 
@@ -270,17 +270,6 @@ cudaError_t launch_gateup_swiglu(const uint32_t* gcodes, const uint16_t* gscales
                                  const uint16_t* uscales, const uint16_t* x, uint16_t* out, int M, int k, int L,
                                  int64_t rows, int64_t cols, cudaStream_t st) {
   if (M == 1) return launch_gateup_swiglu_fma(gcodes, gscales, ucodes, uscales, x, out, M, k, L, rows, cols, st);
-  return tc_dispatch<true>(gcodes, gscales, ucodes, uscales, x, out, M, k, L, rows, cols, st);
-}
-
-cudaError_t launch_matvec_axis1_tc(const uint32_t* codes, const uint16_t* scales, const uint16_t* x, uint16_t* out,
-                                   int M, int k, int L, int64_t rows, int64_t cols, cudaStream_t st) {
-  return tc_dispatch<false>(codes, scales, codes, scales, x, out, M, k, L, rows, cols, st);
-}
-
-cudaError_t launch_gateup_swiglu_tc(const uint32_t* gcodes, const uint16_t* gscales, const uint32_t* ucodes,
-                                    const uint16_t* uscales, const uint16_t* x, uint16_t* out, int M, int k, int L,
-                                    int64_t rows, int64_t cols, cudaStream_t st) {
   return tc_dispatch<true>(gcodes, gscales, ucodes, uscales, x, out, M, k, L, rows, cols, st);
 }
 
