@@ -175,8 +175,15 @@ __global__ void __launch_bounds__(32 * ax0_warps<M>(), 1) ax0_kernel(const Ax0Pa
       if constexpr (BW) sr = *sc;
 #pragma unroll
       for (int i2 = 0; i2 < 8; ++i2) {
-        float2 y = __fadd2_rn(
-            make_float2(__uint_as_float(code_magic(s[2 * i2])), __uint_as_float(code_magic(s[2 * i2 + 1]))), nmagic);
+        // y by an int-to-float conversion on the ALU pipe or by the float-bias subtraction on the FMA pipes (both
+        // exact): the ALU form for every pair at K = 2 and three pairs in four at K = 4, where the window extraction
+        // leaves the ALU pipe room; at K = 3 its funnel shifts fill the ALU pipe and the FMA form stays
+        constexpr bool kAluAll = K == 2, kAluMost = K == 4;
+        const bool alu = kAluAll || (kAluMost && (i2 & 3) != 3);
+        float2 y = alu ? code_y2_alu(s[2 * i2], s[2 * i2 + 1])
+                       : __fadd2_rn(make_float2(__uint_as_float(code_magic(s[2 * i2])),
+                                                __uint_as_float(code_magic(s[2 * i2 + 1]))),
+                                    nmagic);
         if constexpr (BW) {  // bf16(value * scale), the expand weight
           const float2 wv = __fmul2_rn(value_rn2(y), make_float2(sr, sr));
           const uint32_t bb = pack_bf16x2(wv.x, wv.y);
