@@ -21,7 +21,8 @@
 //     x traffic costs one shared-memory wavefront per 4 positions x 32 rows.
 //   * the 1MAD byte sum is one dp4a onto -510 and y an int-to-float
 //     conversion (ALU pipe, leaving the FMA-heavy pipe to the multiply, the
-//     byte sum and the FMAs), and y*x accumulates with packed f32x2 FMA; the
+//     byte sum and the FMAs; at k = 3 half of them take the float-bias
+//     subtraction instead), and y*x accumulates with packed f32x2 FMA; the
 //     per-row factor scale/d is applied once after the reduction (the pages
 //     apply it per weight; the difference is a few fp32 ulp per sum).
 //   * each decoded weight is shared across the M input rows.
@@ -130,8 +131,14 @@ __global__ void __launch_bounds__(512) mv1_kernel(const Mv1Params p) {
         run_states<K, L>(w, s);
 #pragma unroll
         for (int j4 = 0; j4 < 8; ++j4) {
+          // y through the int-to-float conversion (ALU pipe); at K = 3, whose window extraction takes more
+          // ALU work, every second pair through the float-bias subtraction on the FMA pipes instead (exact
+          // either way)
           float2 ya = code_y2_alu(s[4 * j4], s[4 * j4 + 1]);
-          float2 yb = code_y2_alu(s[4 * j4 + 2], s[4 * j4 + 3]);
+          float2 yb = K == 3 ? __fadd2_rn(make_float2(__uint_as_float(code_magic(s[4 * j4 + 2])),
+                                                      __uint_as_float(code_magic(s[4 * j4 + 3]))),
+                                          make_float2(-kMagic, -kMagic))
+                             : code_y2_alu(s[4 * j4 + 2], s[4 * j4 + 3]);
           if constexpr (BW) {
             ya = bf16_weights(ya, wsc[t]);
             yb = bf16_weights(yb, wsc[t]);
