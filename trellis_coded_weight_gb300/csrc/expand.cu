@@ -106,8 +106,12 @@ __global__ void __launch_bounds__(kExpandThreads) expand_kernel(const uint32_t* 
       uint32_t o[8];
 #pragma unroll
       for (int i = 0; i < 16; i += 2) {  // positions 16j + i, 16j + i + 1
-        const float2 y = __fadd2_rn(make_float2(__uint_as_float(code_magic(s[i])), __uint_as_float(code_magic(s[i + 1]))),
-                                    nmagic);
+        // y by the float-bias subtraction on the FMA pipes or, for every second pair at k = 3 and 4, by the
+        // int-to-float conversion on the ALU pipe (both exact): the split that measured fastest per k
+        const float2 y = (K >= 3 && (i & 2) == 0)
+                             ? code_y2_alu(s[i], s[i + 1])
+                             : __fadd2_rn(make_float2(__uint_as_float(code_magic(s[i])), __uint_as_float(code_magic(s[i + 1]))),
+                                          nmagic);
         const float2 v = value_rn2(y);
         const float2 wv = __fmul2_rn(v, sc);
         o[i / 2] = pack_bf16x2(wv.x, wv.y);

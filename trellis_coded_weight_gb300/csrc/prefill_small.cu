@@ -123,8 +123,9 @@ __global__ void __launch_bounds__(kPsThreads, 2)
       sh = window_at<L, NW>(w, (63 - qh) * K);
       sl = window_at<L, NW>(w, (63 - ql) * K);
     }
-    const float2 y = __fadd2_rn(make_float2(__uint_as_float(code_magic(sl)), __uint_as_float(code_magic(sh))),
-                                make_float2(-kMagic, -kMagic));
+    // y through the int-to-float conversion on the ALU pipe (exact), leaving the FMA pipes to the 1MAD
+    // multiply, the byte sum and the value and scale products
+    const float2 y = code_y2_alu(sl, sh);
     const float2 v = __fmul2_rn(value_rn2(y), make_float2(s, s));
     return pack_bf16x2(v.x, v.y);  // low half: position ql
   };
