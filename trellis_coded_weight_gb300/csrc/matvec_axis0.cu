@@ -176,9 +176,10 @@ __global__ void __launch_bounds__(32 * ax0_warps<M>(), 1) ax0_kernel(const Ax0Pa
 #pragma unroll
       for (int i2 = 0; i2 < 8; ++i2) {
         // y by an int-to-float conversion on the ALU pipe or by the float-bias subtraction on the FMA pipes (both
-        // exact): the ALU form for every pair at K = 2 and three pairs in four at K = 4, where the window extraction
-        // leaves the ALU pipe room; at K = 3 its funnel shifts fill the ALU pipe and the FMA form stays
-        constexpr bool kAluAll = K == 2, kAluMost = K == 4;
+        // exact): the ALU form for every pair at K = 2 (L = 16) and three pairs in four at K = 4, where the window
+        // extraction leaves the ALU pipe room; at K = 3 (and K = 2, L = 12) the window extraction fills the ALU
+        // pipe and the FMA form stays
+        constexpr bool kAluAll = K == 2 && L == 16, kAluMost = K == 4;
         const bool alu = kAluAll || (kAluMost && (i2 & 3) != 3);
         float2 y = alu ? code_y2_alu(s[2 * i2], s[2 * i2 + 1])
                        : __fadd2_rn(make_float2(__uint_as_float(code_magic(s[2 * i2])),

@@ -20,8 +20,8 @@
 //   * x is staged once per CTA in shared memory as fp32 (bf16 widened, exact), laid out so that the 8-byte B
 //     fragment loads of the 4*M real lanes fall in distinct banks; lanes of absent tokens read a zero area.
 //   * y comes from the byte sum (dp4a) and an int-to-float conversion (ALU pipe), which leaves the FMA pipes to
-//     the 1MAD multiply and the byte sum; at K = 3, whose window extraction loads the ALU pipe more, one row of
-//     the lane takes the float-bias subtraction (FMA pipe) instead.  With L = 16 and K in {2, 4} one funnel shift
+//     the 1MAD multiply and the byte sum; at K = 3 or L = 12, whose window extraction loads the ALU pipe more,
+//     one row of the lane takes the float-bias subtraction (FMA pipe) instead.  With L = 16 and K in {2, 4} one funnel shift
 //     yields the states of two positions 16 bits apart.
 //   * M = 1 goes to the CUDA-core kernel (matvec_axis1.cu): with one token the packed FMA costs no more than
 //     the MMA, and that kernel stages no x; measured at 17408 x 5120 it is as fast or faster for k = 2..4.
@@ -168,9 +168,9 @@ __global__ void __launch_bounds__(TcCfg<K, L, M, GU>::Threads, 2)
               sa = window_at<L, NW>(w[h], (63 - qa) * K);
               sb = window_at<L, NW>(w[h], (63 - qb) * K);
             }
-            // y through the int-to-float conversion (ALU pipe); at K = 3, whose window extraction takes
-            // more ALU work, row g+8 through the float-bias subtraction (FMA pipe) instead
-            constexpr bool kAluBoth = K != 3;
+            // y through the int-to-float conversion (ALU pipe); at K = 3 or L = 12, whose window extraction
+            // takes more ALU work, row g+8 through the float-bias subtraction (FMA pipe) instead
+            constexpr bool kAluBoth = K != 3 && L == 16;
             fa[h][i] = (h == 0 || kAluBoth) ? code_f32<true>(sa) : code_f32<false>(sa);
             fb[h][i] = (h == 0 || kAluBoth) ? code_f32<true>(sb) : code_f32<false>(sb);
           }

@@ -144,8 +144,12 @@ __global__ void __launch_bounds__(kPaThreads, 1) pa_kernel(const PaParams p) {
   // the weights of rows ra (low half) and ra+1 (high half) at the output of state pair (sa, sb), packed bf16
   auto pair_w = [&](uint32_t sa, uint32_t sb, float2 sc) -> uint32_t {
     // y through the int-to-float conversion on the ALU pipe (exact), leaving the FMA pipes to the 1MAD
-    // multiply, the byte sum and the value and scale products
-    const float2 y = code_y2_alu(sa, sb);
+    // multiply, the byte sum and the value and scale products; at K = 2 with L = 12 windows the float-bias
+    // subtraction on the FMA pipes measured faster
+    constexpr bool kAlu = !(K == 2 && L == 12);
+    const float2 y = kAlu ? code_y2_alu(sa, sb)
+                          : __fadd2_rn(make_float2(__uint_as_float(code_magic(sa)), __uint_as_float(code_magic(sb))),
+                                       make_float2(-kMagic, -kMagic));
     const float2 v = __fmul2_rn(value_rn2(y), sc);
     return pack_bf16x2(v.x, v.y);
   };
