@@ -54,8 +54,8 @@ sys.path.insert(0, ROOT)
 METRIC = "packed-weight HBM GB/s (frac of GB300 peak) at M=1..4; prefill TFLOP/s at M=2048"
 R, C, L, T = 17408, 5120, 16, 256
 KS, MS = (2, 3, 4), (1, 2, 3, 4)
-PREFILL_M = (8, 16, 32, 512, 2048)  # 8 and 16: the register-decode path; 32 and up: tcgen05
-PREFILL0_M = (8, 64, 512, 2048)
+PREFILL_M = (8, 16, 24, 32, 512, 2048)  # up to 24: the register-decode path; 32 and up: tcgen05
+PREFILL0_M = (8, 32, 64, 512, 2048)  # up to 32: the register-decode path; 64 and up: tcgen05
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 

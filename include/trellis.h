@@ -259,9 +259,9 @@ int trellis_mlp_decode(const uint32_t *gcodes, const uint16_t *gscales, const ui
  * rows and stored transposed into the tile, and the long reduction over rows
  * is split across thread-block clusters where tiles alone would leave SMs
  * idle (possibly as a second launch on `stream` for the tiles left after
- * whole waves).  With M <= 16 the decoded weights stay in registers instead
- * and warp-level MMAs (mma.sync bf16, one or two 8-token tiles) multiply
- * them: the same numerics, no shared-memory weight tiles; on axis 0 a
+ * whole waves).  With M <= 24 on axis 1 and M <= 32 on axis 0 the decoded
+ * weights stay in registers instead and warp-level MMAs (mma.sync bf16, one
+ * to four 8-token tiles) multiply them: the same numerics, no shared-memory weight tiles; on axis 0 a
  * thread-block cluster splits each 256-output block's reduction and folds
  * it through distributed shared memory.  Results
  * are deterministic: repeated calls give equal bits.
@@ -309,7 +309,8 @@ int trellis_load_floor_rows(const uint32_t *codes, uint32_t *out, const trellis_
  * t % ceil(features/128), token tile t / ceil(features/128).
  *   launches: caller-owned, room for 2 launches (6 ints).
  * Returns the number of launches (1 or 2); 0, with *tokens_per_tile = 0,
- * when the call has no tiles: with M <= 16 trellis_gemm_prefill decodes
+ * when the call has no tiles: with M <= 24 (axis 1) or M <= 32 (axis 0)
+ * trellis_gemm_prefill decodes
  * into registers and multiplies with warp-level MMAs instead (axis 1: 64
  * rows per thread block; axis 0: a thread-block cluster per 256 outputs).  Or a negative status: the geometry and M checks
  * of trellis_gemm_prefill, ENULL, or EDEVICE when sms < 1 and no usable

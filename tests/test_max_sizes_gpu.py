@@ -131,9 +131,9 @@ def test_axis0_matvec_past_2e31_words(oracle_mod, big, M):
     check_band(oracle_mod, out[:, glob], ref, ab, f"axis0 past 2^31 words M={M}")
 
 
-@pytest.mark.parametrize("M", [8, 24])
+@pytest.mark.parametrize("M", [8, 32, 40])
 def test_axis0_prefill_past_2e31_words(oracle_mod, big, M):
-    """M = 8 on the register-decode kernel (cluster fold), M = 24 on the tcgen05 kernel."""
+    """M = 8 and 32 on the register-decode kernel (cluster fold), M = 40 on the tcgen05 kernel."""
     base, codes, scales, d_scales, _, _ = big
     g = tb.Geometry(Big.k, L, T, 0, Big.rows, Big.cols)
     x = inputs.normal_bf16(7500 + M, (M, Big.rows), 0.5)

@@ -24,6 +24,7 @@ def _lib():
 
 @pytest.mark.parametrize("k", [2, 3, 4])
 @pytest.mark.parametrize("M,rows,cols", [(1, 64, 512), (5, 128, 256), (12, 77, 512), (16, 200, 5120), (17, 130, 768),
+                                         (24, 77, 1024), (25, 130, 512),
                                          (32, 200, 768), (33, 128, 512), (100, 257, 1024),
                                          (300, 136, 512), (64, 64, 2048), (600, 130, 1024)])
 def test_prefill_small(oracle_mod, k, M, rows, cols):
@@ -68,7 +69,7 @@ def test_prefill_L12(oracle_mod):
 
 @pytest.mark.parametrize("k", [2, 3, 4])
 def test_prefill_small_M_L12(oracle_mod, k):
-    """The register-decode path (axis 1, M <= 16) with 12-bit windows: neighbouring positions pair up."""
+    """The register-decode path (axis 1, M <= 24) with 12-bit windows: neighbouring positions pair up."""
     codes, scales, x = inputs.make_linear(70, 768, k, 9, seed_codes=5 + k)
     g = tb.Geometry(k, 12, T, 1, 70, 768)
     out = tb.gemm_prefill(to_dev_u32(codes), to_dev_f16(scales), to_dev_bf16(x), g)
@@ -76,7 +77,7 @@ def test_prefill_small_M_L12(oracle_mod, k):
     check_band(oracle_mod, bf16_bits(out), ref, ab, f"prefill L=12 k={k} M=9")
 
 
-@pytest.mark.parametrize("M", [8, 16])
+@pytest.mark.parametrize("M", [8, 16, 24])
 def test_prefill_small_M_full_size_sampled(oracle_mod, M):
     rows, cols = 17408, 5120
     codes, scales, x = inputs.make_linear(rows, cols, 2, M)
@@ -89,6 +90,7 @@ def test_prefill_small_M_full_size_sampled(oracle_mod, M):
 
 @pytest.mark.parametrize("k", [2, 3, 4])
 @pytest.mark.parametrize("M,rows,cols", [(1, 64, 256), (5, 256, 256), (8, 1000, 512), (12, 8, 256), (16, 520, 768),
+                                         (17, 1000, 512), (24, 520, 768), (32, 8, 256), (32, 1000, 1024),
                                          (40, 1000, 512), (300, 520, 768), (33, 8, 256)])
 def test_prefill_axis0_small(oracle_mod, k, M, rows, cols):
     """Axis 0 (stored W^T): out[m][c] = sum_r e(r,c) x[m][r] over bf16 expand weights."""
@@ -100,16 +102,17 @@ def test_prefill_axis0_small(oracle_mod, k, M, rows, cols):
 
 
 @pytest.mark.parametrize("k", [2, 3, 4])
-def test_prefill_axis0_small_M_L12(oracle_mod, k):
-    """The register-decode path of axis 0 (M <= 16) with 12-bit windows."""
-    codes, scales, x = inputs.make_linear(296, 512, k, 11, seed_codes=9 + k, seed_x=10, sigma=0.5, x_len=296)
+@pytest.mark.parametrize("M", [11, 28])
+def test_prefill_axis0_small_M_L12(oracle_mod, k, M):
+    """The register-decode path of axis 0 (M <= 32) with 12-bit windows."""
+    codes, scales, x = inputs.make_linear(296, 512, k, M, seed_codes=9 + k, seed_x=10, sigma=0.5, x_len=296)
     g = tb.Geometry(k, 12, T, 0, 296, 512)
     out = tb.gemm_prefill(to_dev_u32(codes), to_dev_f16(scales), to_dev_bf16(x), g)
     ref, ab = oracle_mod.matvec_axis0_bf16w(codes, scales, x, k, 12, T)
-    check_band(oracle_mod, bf16_bits(out), ref, ab, f"prefill axis0 L=12 k={k} M=11")
+    check_band(oracle_mod, bf16_bits(out), ref, ab, f"prefill axis0 L=12 k={k} M={M}")
 
 
-@pytest.mark.parametrize("M", [8, 16])
+@pytest.mark.parametrize("M", [8, 16, 24, 32])
 def test_prefill_axis0_small_M_full_size_sampled(oracle_mod, M):
     """The down projection (17408 stored rows, 5120 outputs) at small M: 20 column blocks, each a cluster whose
     CTAs split the 17408 rows and fold their partials; sampled outputs against the oracle, repeated calls equal."""
@@ -189,12 +192,12 @@ def test_prefill_axis0_leftover_tiles_one_stage(oracle_mod):
 
 # ------------------------------------------------------------------ bounded waits (failure detection)
 
-@pytest.mark.parametrize("axis,M", [(1, 40), (0, 24)])
+@pytest.mark.parametrize("axis,M", [(1, 40), (0, 40)])
 def test_bounded_waits_run_out_and_the_next_call_is_correct(oracle_mod, axis, M):
     """Failure detection without a GPU fault: with every pipeline wait limited to 200 ns the waits of an
     ordinary problem run out; the kernel records a non-zero error word, lets its copies and MMAs finish and
     returns with the context intact.  The next call, at the default limit, is correct and clean.  Axis 0 at
-    M = 24 runs the cluster-split reduction (8-CTA clusters), whose waits run out too."""
+    M = 40 runs the cluster-split reduction (8-CTA clusters), whose waits run out too."""
     rows, cols, k = 512, 2048, 2
     codes, scales, _ = inputs.make_linear(rows, cols, k, 1, seed_codes=880 + axis, seed_scales=881)
     n_in = cols if axis == 1 else rows

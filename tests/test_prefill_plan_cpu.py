@@ -39,22 +39,30 @@ def _stages(M, g):
     return -(-kd // bk)
 
 
-@pytest.mark.parametrize("M,tokens", [(17, 32), (32, 32), (33, 64), (64, 64), (65, 128), (128, 128),
+@pytest.mark.parametrize("M,tokens", [(25, 32), (32, 32), (33, 64), (64, 64), (65, 128), (128, 128),
                                       (129, 256), (256, 256), (257, 512), (2048, 512), (100000, 512)])
 def test_tokens_per_tile(M, tokens):
     bn, _ = tb.prefill_plan(M, tb.Geometry(2, 16, 256, 1, 17408, 5120), 152)
     assert bn == tokens
-    assert tb.prefill_plan(M, tb.Geometry(2, 16, 256, 0, 17408, 5120), 152)[0] == tokens
+    if M > 32:  # axis 0 keeps the register-decode kernel up to 32 tokens
+        assert tb.prefill_plan(M, tb.Geometry(2, 16, 256, 0, 17408, 5120), 152)[0] == tokens
 
 
-@pytest.mark.parametrize("M", [1, 5, 16])
+SMALL_M_MAX = {1: 24, 0: 32}  # the register-decode kernels' range per axis
+
+
+@pytest.mark.parametrize("M", [1, 5, 16, 17, 24, 25, 32, 33])
 @pytest.mark.parametrize("axis", [0, 1])
 def test_small_M_has_no_tiles(M, axis):
-    # M <= 16 runs the register-decode kernels on either axis: no tile plan
-    assert tb.prefill_plan(M, tb.Geometry(2, 16, 256, axis, 17408, 5120), 152) == (0, [])
+    # up to 24 tokens on axis 1 and 32 on axis 0 the register-decode kernels run: no tile plan
+    bn, plan = tb.prefill_plan(M, tb.Geometry(2, 16, 256, axis, 17408, 5120), 152)
+    if M <= SMALL_M_MAX[axis]:
+        assert (bn, plan) == (0, [])
+    else:
+        assert bn == (32 if M <= 32 else 64) and len(plan) >= 1
 
 
-@pytest.mark.parametrize("M", [17, 32, 512, 2048, 5000])
+@pytest.mark.parametrize("M", [25, 32, 512, 2048, 5000])
 def test_axis1_is_one_persistent_launch(M):
     g = tb.Geometry(2, 16, 256, 1, 17408, 5120)
     _, plan = tb.prefill_plan(M, g, 152)
@@ -64,7 +72,8 @@ def test_axis1_is_one_persistent_launch(M):
 def test_axis0_pages_shapes():
     # the down projection, stored W^T [17408 in][5120 out]: 40 feature tiles
     g = tb.Geometry(3, 16, 256, 0, 17408, 5120)
-    assert tb.prefill_plan(24, g, 152) == (32, [(0, 40, 3)])      # 3 CTAs per tile fill 120 of 152 SMs
+    assert tb.prefill_plan(24, g, 152) == (0, [])                 # the register-decode kernel up to 32 tokens
+    assert tb.prefill_plan(40, g, 152) == (64, [(0, 40, 3)])      # 3 CTAs per tile fill 120 of 152 SMs
     assert tb.prefill_plan(64, g, 152) == (64, [(0, 40, 3)])
     assert tb.prefill_plan(512, g, 152) == (512, [(0, 40, 3)])
     assert tb.prefill_plan(1024, g, 152) == (512, [(0, 80, 1)])   # 80 tiles: no room for 2 CTAs each
@@ -83,7 +92,7 @@ def test_split_caps():
     assert tb.prefill_plan(600, g, 100)[1] == [(0, 16, 6)]        # 16 tiles x 6 CTAs fill 96 of 100 SMs
     short = tb.Geometry(3, 16, 256, 0, 96, 5376)                  # 96 rows: 3 stages of 32 at BN = 512
     assert tb.prefill_plan(1600, short, 152) == (512, [(0, 152, 1), (152, 16, 3)])
-    assert tb.prefill_plan(24, tb.Geometry(2, 16, 256, 0, 64, 5120), 152)[1] == [(0, 40, 1)]  # 1 stage of 64
+    assert tb.prefill_plan(40, tb.Geometry(2, 16, 256, 0, 64, 5120), 152)[1] == [(0, 40, 1)]  # 1 stage of 64
 
 
 @pytest.mark.parametrize("sms", [1, 7, 132, 148, 152, 160])
@@ -95,7 +104,7 @@ def test_plan_invariants(sms, axis):
         g = tb.Geometry(3, 16, 256, axis, rows, cols)
         for M in (1, 31, 64, 200, 300, 512, 777, 1024, 2048, 4096):
             bn, plan = tb.prefill_plan(M, g, sms)
-            if M <= 16:  # the register-decode kernels: no tiles
+            if M <= SMALL_M_MAX[axis]:  # the register-decode kernels: no tiles
                 assert (bn, plan) == (0, [])
                 continue
             _, ntiles = _tiles(M, g)

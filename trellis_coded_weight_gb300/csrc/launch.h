@@ -60,10 +60,13 @@ cudaError_t launch_matvec_axis0_fma(const uint32_t* codes, const uint16_t* scale
 cudaError_t launch_gemm_prefill(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
                                 uint16_t* out, int M, int k, int L, int axis, int64_t rows, int64_t cols,
                                 cudaStream_t st);
-// The prefill for M <= kPrefillSmallMaxM: the decode in registers and mma.sync bf16, on axis 1
-// (prefill_small.cu) and on axis 0 (prefill_axis0_small.cu, clusters folding the split reduction); launch_gemm_prefill
-// takes them for those M.
-constexpr int kPrefillSmallMaxM = 16;
+// The prefill for small M: the decode in registers and mma.sync bf16 (up to four 8-token tiles), on axis 1
+// (prefill_small.cu) and on axis 0 (prefill_axis0_small.cu, clusters folding the split reduction);
+// launch_gemm_prefill takes them up to the measured crossovers with the tcgen05 kernel: 24 tokens on axis 1,
+// 32 on axis 0.
+constexpr int kPrefillSmallMaxM1 = 24;
+constexpr int kPrefillSmallMaxM0 = 32;
+constexpr int prefill_small_max_m(int axis) { return axis == 1 ? kPrefillSmallMaxM1 : kPrefillSmallMaxM0; }
 cudaError_t launch_prefill_small(const uint32_t* codes, const uint16_t* scales, const uint16_t* x, uint16_t* out,
                                  int M, int k, int L, int64_t rows, int64_t cols, cudaStream_t st);
 cudaError_t launch_prefill_axis0_small(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
@@ -74,7 +77,7 @@ cudaError_t launch_prefill_axis0_small(const uint32_t* codes, const uint16_t* sc
 // to two launches over the output tiles, each [t0, t0 + count) with S CTAs per
 // tile (S > 1: a cluster splitting the tile's reduction).  Returns the number
 // of launches; 0 (and 0 tokens per tile) where the call takes a
-// register-decode kernel instead (M <= kPrefillSmallMaxM).
+// register-decode kernel instead (M <= prefill_small_max_m(axis)).
 struct PrefillLaunch {
   int t0, count, S;
 };

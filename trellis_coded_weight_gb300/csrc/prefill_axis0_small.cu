@@ -1,4 +1,4 @@
-// prefill_axis0_small.cu -- the axis-0 prefill GEMM (a stored W^T, the down projection) for small M (M <= 16):
+// prefill_axis0_small.cu -- the axis-0 prefill GEMM (a stored W^T, the down projection) for small M (M <= 32):
 //   out[m][c] = bf16( sum_r w(r,c) x[m][r] ),  w = bf16(fl32(value * scale[r])), the expand weight,
 // accumulated in fp32 ("trellis-splitk-prefill.ts" diff page: the reduction over stored rows split across
 // workers and the partials summed; "trellis-vector-expand.ts" for the weight).
@@ -300,7 +300,12 @@ cudaError_t pa_launch(const PaParams& p0, cudaStream_t st) {
 
 template <int K, int L>
 cudaError_t pa_launch_nt(const PaParams& p, cudaStream_t st) {
-  return p.M <= 8 ? pa_launch<K, L, 1>(p, st) : pa_launch<K, L, 2>(p, st);
+  switch ((p.M + 7) / 8) {  // 8-token tiles
+    case 1: return pa_launch<K, L, 1>(p, st);
+    case 2: return pa_launch<K, L, 2>(p, st);
+    case 3: return pa_launch<K, L, 3>(p, st);
+    default: return pa_launch<K, L, 4>(p, st);
+  }
 }
 
 }  // namespace
@@ -308,7 +313,7 @@ cudaError_t pa_launch_nt(const PaParams& p, cudaStream_t st) {
 cudaError_t launch_prefill_axis0_small(const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
                                        uint16_t* out, int M, int k, int L, int64_t rows, int64_t cols,
                                        cudaStream_t st) {
-  if (M < 1 || M > kPrefillSmallMaxM || rows % 8 != 0) return cudaErrorInvalidValue;
+  if (M < 1 || M > kPrefillSmallMaxM0 || rows % 8 != 0) return cudaErrorInvalidValue;
   PaParams p{};
   p.codes = codes; p.scales = scales; p.x = x; p.out = out;
   p.R = rows; p.C = cols; p.M = M; p.nb = (int)(cols / kT); p.S = 1;

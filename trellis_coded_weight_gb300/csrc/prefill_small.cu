@@ -1,11 +1,12 @@
-// prefill_small.cu -- the axis-1 prefill GEMM for small M (M <= 16): out[m][r] = bf16( sum_c w(r,c) x[m][c] )
+// prefill_small.cu -- the axis-1 prefill GEMM for small M (M <= 24): out[m][r] = bf16( sum_c w(r,c) x[m][c] )
 // with the prefill's weight numerics w = bf16(fl32(value * scale[r])), the expand weight ("trellis-tiled-prefill.ts"
 // diff page: decode into the tile, then the matrix product; "trellis-vector-expand.ts" for the weight).
 //
 // GB300 design.  At small M the tcgen05 prefill spends its time writing every decoded weight through shared memory
 // for a narrow MMA, on 136 row tiles of 128 rows (16 of 152 SMs idle).  Here the decode stays in registers, as in
 // the tensor-core matvec (matvec_axis1_tc.cu), and the products go through mma.sync m16n8k16 bf16 with one 8-token
-// tile per 8 tokens (the kernel takes up to four; the launcher routes M <= 16 here):
+// tile per 8 tokens (the kernel takes up to four; the launcher routes M <= 24 here, below its measured crossover
+// with the tcgen05 kernel between 24 and 28 tokens):
 //   * a CTA owns 64 rows (four 16-row groups) and the row's blocks split over KS warps per group; lane (g, t)
 //     decodes rows g and g+8 of its group at positions [64t, 64t+64) of a block from 2K words (16-byte loads) and
 //     the spill word of the neighbouring lane (a shuffle).
@@ -275,7 +276,7 @@ cudaError_t pfs_launch_nt(const uint32_t* codes, const uint16_t* scales, const u
 
 cudaError_t launch_prefill_small(const uint32_t* codes, const uint16_t* scales, const uint16_t* x, uint16_t* out, int M,
                                  int k, int L, int64_t rows, int64_t cols, cudaStream_t st) {
-  if (M < 1 || M > kPrefillSmallMaxM) return cudaErrorInvalidValue;
+  if (M < 1 || M > kPrefillSmallMaxM1) return cudaErrorInvalidValue;
   if (L == 16) {
     if (k == 2) return pfs_launch_nt<2, 16>(codes, scales, x, out, M, rows, cols, st);
     if (k == 3) return pfs_launch_nt<3, 16>(codes, scales, x, out, M, rows, cols, st);

@@ -839,7 +839,7 @@ cudaError_t prefill_axis(const PrefillParams& p, const uint16_t* x, int k, int L
 int device_sm_count() { return sm_count(); }
 
 int prefill_plan(int M, int axis, int64_t nOut, int64_t Kd, int sms, int* tokens_per_tile, PrefillLaunch* launches) {
-  if (M <= kPrefillSmallMaxM) {  // no tiles: the register-decode kernels (prefill_small.cu, prefill_axis0_small.cu)
+  if (M <= prefill_small_max_m(axis)) {  // no tiles: the register-decode kernels (prefill_small.cu, prefill_axis0_small.cu)
     *tokens_per_tile = 0;
     return 0;
   }
@@ -868,7 +868,7 @@ int prefill_plan(int M, int axis, int64_t nOut, int64_t Kd, int sms, int* tokens
 
 cudaError_t launch_gemm_prefill(const uint32_t* codes, const uint16_t* scales, const uint16_t* x, uint16_t* out,
                                 int M, int k, int L, int axis, int64_t rows, int64_t cols, cudaStream_t st) {
-  if (M <= kPrefillSmallMaxM)
+  if (M <= prefill_small_max_m(axis))
     return axis == 1 ? launch_prefill_small(codes, scales, x, out, M, k, L, rows, cols, st)
                      : launch_prefill_axis0_small(codes, scales, x, out, M, k, L, rows, cols, st);
   PrefillParams p{};
