@@ -17,8 +17,8 @@ prefill (k = 3, M = 8 / 64 / 512 / 2048, next to expand + cuBLAS), the decode
 MLP block as a CUDA graph, and two load-only floors of the packed stream.
 
 `e2e` is the headline's twelve launches through trellis_matvec_axis1_host, one
-C call per launch that copies its x in from pinned host memory and its output
-back, on one stream; `e2e.two_streams` the same calls alternating between two
+C call per launch that brings its x in from pinned host memory and its output
+back (through the buffers' device mapping), on one stream; `e2e.two_streams` the same calls alternating between two
 streams.  `roofline` is the axis-1 matvec's: algorithmic bytes per launch over
 the timed region's mean launch time, against the measured HBM copy rate.
 
@@ -301,8 +301,9 @@ def run_gpu(args):
 
 def run_e2e(args, torch, tdist, tb, dev, stream, bufs, scales, geoms, xs, rot, world, sync_all):
     """The headline through the C ABI with host buffers: each launch is one trellis_matvec_axis1_host call, which
-    queues the copy of its x from pinned host memory, the matvec and the copy of its output back to pinned host
-    memory, in order on its stream.  Each (k, M) slot has its own host and device buffers; the arguments are
+    queues the copy of its x from pinned host memory, the matvec and the transfer of its output back to pinned host
+    memory, in order on its stream (pinned buffers are reached through their device mapping: a fetch kernel brings
+    x in over the host link and the matvec stores its output straight into host memory).  Each (k, M) slot has its own host and device buffers; the arguments are
     prepared once (pointers, geometry, stream), as for the device-timed headline.
 
     `value` runs every call on the launching stream, so the matvecs run one after another as in the

@@ -116,15 +116,20 @@ int trellis_matvec_axis1(const uint32_t *codes, const uint16_t *scales, const ui
 /*
  * trellis_matvec_axis1_host -- trellis_matvec_axis1 with x and out in host
  * memory: one call queues, in order on `stream`, the copy of x_host
- * [M][cols] bf16 into the caller's device buffer x_dev, the matvec into the
- * caller's device buffer out_dev [M][rows], and the copy of out_dev into
- * out_host.  It returns once they are queued; out_host holds the result when
- * the stream has reached that point (synchronize the stream or an event
- * recorded after the call).  The pages' decode call does the same for one
- * token: its input arrives from the host and its output goes back.
- *   x_host, out_host: host memory, no alignment rule; pinned memory
- *   (cudaHostAlloc / cudaHostRegister) keeps the copies asynchronous, pageable
- *   memory is copied through a driver staging buffer and the call may block.
+ * [M][cols] bf16 into the caller's device buffer x_dev, the matvec, and the
+ * transfer of its output [M][rows] into out_host.  It returns once they are
+ * queued; out_host holds the result when the stream has reached that point
+ * (synchronize the stream or an event recorded after the call).  The pages'
+ * decode call does the same for one token: its input arrives from the host
+ * and its output goes back.
+ *   x_host, out_host: host memory, no alignment rule.  Pinned memory
+ *   (cudaHostAlloc / cudaHostRegister) mapped into the device's address space
+ *   and 16-byte aligned is reached through that mapping: a small kernel copies
+ *   x_host into x_dev and the matvec stores its output straight into out_host
+ *   (out_dev is then not written).  Other host memory goes through the copy
+ *   engines: x_host into x_dev, the matvec into out_dev, out_dev into
+ *   out_host; pageable memory is copied through a driver staging buffer and
+ *   the call may block.
  *   x_dev, out_dev: device memory, 16-byte aligned, owned by the caller; they
  *   must not be in use by other work until the stream has passed the call.
  *   codes, scales, M, g: as for trellis_matvec_axis1.

@@ -104,6 +104,58 @@ def test_matvec_axis1_host_buffers(oracle_mod, M, pinned):
     check_band(oracle_mod, bf16_bits(out_host), ref, ab, f"axis1 host buffers M={M}")
 
 
+def _host_view(a: np.ndarray, pinned: bool, shift: int) -> torch.Tensor:
+    """A bf16 host tensor holding `a`'s bits, `shift` elements into its (pinned or pageable) allocation."""
+    flat = torch.empty(a.size + shift, dtype=torch.int16)
+    if pinned:
+        flat = flat.pin_memory()
+    v = flat[shift:].view(a.shape)
+    v.copy_(torch.from_numpy(a.view(np.int16)))
+    return v.view(torch.bfloat16)
+
+
+@pytest.mark.parametrize("x_pinned,out_pinned,shift", [
+    (True, False, 0), (False, True, 0),  # one side through its mapping, the other through the copy engines
+    (True, True, 8),                     # 16 bytes into a pinned allocation: the mapping's offset
+    (True, True, 1),                     # 2 bytes in: not 16-byte aligned, the copy engines
+])
+def test_matvec_axis1_host_buffer_forms(oracle_mod, x_pinned, out_pinned, shift):
+    """Every combination of how the host call reaches x_host and out_host gives the device call's bits."""
+    rows, cols, k, M = 272, 1536, 2, 3
+    codes, scales, x = inputs.make_linear(rows, cols, k, M, seed_codes=93, seed_x=94)
+    g = tb.Geometry(k, L, T, 1, rows, cols)
+    dc, ds = to_dev_u32(codes), to_dev_f16(scales)
+    x_host = _host_view(x, x_pinned, shift)
+    out_host = _host_view(np.full((M, rows), 0xBF80, dtype=np.uint16), out_pinned, shift)
+    x_dev = torch.empty((M, cols), dtype=torch.bfloat16, device="cuda")
+    out_dev = torch.empty((M, rows), dtype=torch.bfloat16, device="cuda")
+    tb.matvec_axis1_host(dc, ds, x_host, g, out_host, x_dev, out_dev)
+    torch.cuda.current_stream().synchronize()
+    dev = tb.matvec_axis1(dc, ds, to_dev_bf16(x), g)
+    assert torch.equal(out_host.view(torch.int16), dev.cpu().view(torch.int16))
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+def test_matvec_axis1_host_chain_reuses_buffers(pinned):
+    """Calls queued back to back without a synchronisation, each taking the previous call's host output as its
+    input and sharing one pair of device buffers: stream order holds (each call reads what the previous call
+    wrote), as in a chain of device calls."""
+    n, k, M, calls = 512, 3, 2, 4
+    codes, scales, x = inputs.make_linear(n, n, k, M, seed_codes=95, seed_x=96)
+    g = tb.Geometry(k, L, T, 1, n, n)
+    dc, ds = to_dev_u32(codes), to_dev_f16(scales)
+    bufs = [_host_view(x if i == 0 else np.zeros((M, n), dtype=np.uint16), pinned, 0) for i in range(calls + 1)]
+    x_dev = torch.empty((M, n), dtype=torch.bfloat16, device="cuda")
+    out_dev = torch.empty((M, n), dtype=torch.bfloat16, device="cuda")
+    for i in range(calls):
+        tb.matvec_axis1_host(dc, ds, bufs[i], g, bufs[i + 1], x_dev, out_dev)
+    torch.cuda.current_stream().synchronize()
+    want = to_dev_bf16(x)
+    for i in range(calls):
+        want = tb.matvec_axis1(dc, ds, want, g)
+        assert torch.equal(bufs[i + 1].view(torch.int16), want.cpu().view(torch.int16)), f"call {i}"
+
+
 @pytest.mark.parametrize("k", [2, 3, 4])
 def test_matvec_axis1_full_size_sampled(oracle_mod, k):
     rows, cols, M = 17408, 5120, 4

@@ -118,10 +118,19 @@ int trellis_matvec_axis1_host(const uint32_t* codes, const uint16_t* scales, con
   if ((st = device_ok())) return st;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t xb = (size_t)M * (size_t)g->cols * sizeof(uint16_t), ob = (size_t)M * (size_t)g->rows * sizeof(uint16_t);
-  if (cudaMemcpyAsync(x_dev, x_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess) return TRELLIS_ECUDA;
-  if (trellis::launch_matvec_axis1(codes, scales, x_dev, out_dev, M, g->k, g->L, g->rows, g->cols, s) != cudaSuccess)
+  // Pinned, 16-byte aligned host buffers are reached through their device mapping: x by a fetch kernel, the
+  // output by the matvec's own stores.  Anything else goes through the copy engines.
+  const void* xv = aligned16(x_host) ? trellis::mapped_host_view(x_host) : nullptr;
+  void* ov = aligned16(out_host) ? const_cast<void*>(trellis::mapped_host_view(out_host)) : nullptr;
+  if (xv && !aligned16(xv)) xv = nullptr;
+  if (ov && !aligned16(ov)) ov = nullptr;
+  const cudaError_t ex = xv ? trellis::launch_fetch16(x_dev, xv, xb, s)
+                            : cudaMemcpyAsync(x_dev, x_host, xb, cudaMemcpyHostToDevice, s);
+  if (ex != cudaSuccess) return TRELLIS_ECUDA;
+  uint16_t* o = ov ? static_cast<uint16_t*>(ov) : out_dev;
+  if (trellis::launch_matvec_axis1(codes, scales, x_dev, o, M, g->k, g->L, g->rows, g->cols, s) != cudaSuccess)
     return TRELLIS_ECUDA;
-  return cuda_status(cudaMemcpyAsync(out_host, out_dev, ob, cudaMemcpyDeviceToHost, s));
+  return ov ? TRELLIS_OK : cuda_status(cudaMemcpyAsync(out_host, out_dev, ob, cudaMemcpyDeviceToHost, s));
 }
 
 int trellis_matvec_axis1_bf16w(const uint32_t* codes, const uint16_t* scales, const uint16_t* x, uint16_t* out,

@@ -41,6 +41,13 @@ cudaError_t launch_gateup_swiglu(const uint32_t* gcodes, const uint16_t* gscales
                                  const uint16_t* uscales, const uint16_t* x, uint16_t* out, int M, int k,
                                  int L, int64_t rows, int64_t cols, cudaStream_t st);
 
+// Host buffers (host_io.cu).  mapped_host_view: the device address of pinned host memory mapped into the
+// current device's address space, or nullptr (pageable memory, no mapping, a failed query).  launch_fetch16:
+// copies `bytes` (a multiple of 16; both addresses 16-byte aligned) from such a mapping into device memory with a
+// kernel launched behind the stream's previous kernel by programmatic dependent launch.
+const void* mapped_host_view(const void* host);
+cudaError_t launch_fetch16(void* dst, const void* src_view, size_t bytes, cudaStream_t st);
+
 // Workspace of the axis-0 matvec: fp32 partials followed by per-column-block
 // arrival counters.  launch_matvec_axis0 takes the tensor-core kernel for M >= 3
 // and the CUDA-core kernel for M <= 2.
