@@ -12,8 +12,8 @@ The same run times every other row of the hot path at its full size, each in
 FLOPs and its fraction of the measured peak: the fused gate/up SwiGLU layer
 (two 17408 x 5120 matrices, k = 2, 3), the axis-0 down projection (stored
 W^T 17408 x 5120, k = 2, 3), the bf16 expansion (k = 2..4), the prefill GEMM
-(k = 2, M = 8 / 16 / 32 / 512 / 2048, next to expand + cuBLAS), the axis-0
-prefill (k = 3, M = 8 / 64 / 512 / 2048, next to expand + cuBLAS), the decode
+(k = 2, M = 8 / 16 / 24 / 32 / 512 / 2048, next to expand + cuBLAS), the axis-0
+prefill (k = 3, M = 8 / 32 / 64 / 512 / 2048, next to expand + cuBLAS), the decode
 MLP block as a CUDA graph, and two load-only floors of the packed stream.
 
 `e2e` is the headline's twelve launches through trellis_matvec_axis1_host, one
