@@ -207,9 +207,11 @@ def _req_host(t: torch.Tensor, name: str, shape):
 
 
 def matvec_axis1_host(codes, scales, x_host, g: Geometry, out_host, x_dev, out_dev):
-    """matvec_axis1 with x and out on the host: one C call queues x_host -> x_dev, the matvec into out_dev and
-    out_dev -> out_host on the current stream of the codes' device.  out_host holds the result once that stream
-    has reached the call (synchronize before reading it).  Pinned host tensors keep the copies asynchronous."""
+    """matvec_axis1 with x and out on the host: one C call queues x_host -> x_dev, the matvec and its output's
+    transfer to out_host on the current stream of the codes' device.  out_host holds the result once that stream
+    has reached the call (synchronize before reading it).  Pinned (16-byte aligned) host tensors are reached
+    through their device mapping: a copy kernel fills x_dev and the matvec writes out_host directly, leaving
+    out_dev untouched; other host tensors go through copy-engine copies via x_dev and out_dev."""
     M = x_host.shape[0]
     args = (_req(codes, "codes", _CODES, g.codes_shape),
             _req(scales, "scales", (torch.float16,), (g.rows,)),
